@@ -1,0 +1,518 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests re-derives the oracle's own formulas and compares the
+two: each checks a property that holds independently of how the oracle is
+written -- the exact output distribution (brute force and chi-square), the
+equivalence of greedy verification with plain greedy decoding, the worked
+examples printed on the pages, the library softmax, and the accept rule's
+special cases.  A negative control shows the exactness checks do catch the
+literal "correction sampled from the target" reading.
+"""
+import itertools
+import json
+import os
+import zlib
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# softmax: a special case that reduces to a library routine
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("V", [1, 2, 7, 1000, 32000])
+@pytest.mark.parametrize("T", [1.0, 0.7, 2.3])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_softmax_matches_library(V, T, dtype):
+    g = torch.Generator().manual_seed(V * 7 + int(T * 10))
+    x = torch.randn(V, generator=g) * 4.0
+    if V > 3:
+        x[1] = float("-inf")
+    if dtype == "bf16":
+        xb = x.to(torch.bfloat16)
+        arr = xb.view(torch.int16).numpy().view(np.uint16)
+        xd = xb.double()
+    else:
+        arr = x.numpy()
+        xd = x.double()
+    p = oracle.softmax_ref(arr, T)
+    ref = torch.softmax(xd / T, dim=0).numpy()
+    np.testing.assert_allclose(p, ref, rtol=1e-12, atol=1e-15)
+    assert abs(p.sum() - 1.0) < 1e-12
+
+
+def test_softmax_rejects_nan_and_inf():
+    with pytest.raises(ValueError):
+        oracle.softmax_ref(np.array([0.0, np.nan, 1.0], np.float32))
+    with pytest.raises(ValueError):
+        oracle.softmax_ref(np.array([0.0, np.inf, 1.0], np.float32))
+    with pytest.raises(ValueError):
+        oracle.softmax_ref(np.array([-np.inf, -np.inf], np.float32))
+
+
+# --------------------------------------------------------------------------
+# exactness by brute force (V <= 4, K <= 2)
+# --------------------------------------------------------------------------
+def _tables(V, K, seed, T):
+    """Prefix-indexed logit tables: target rows for prefixes of length 0..K,
+    draft rows for prefixes of length 0..K-1.  Some tokens get -inf."""
+    rng = np.random.default_rng(seed)
+    tgt, drf = {}, {}
+    for L in range(K + 1):
+        for pre in itertools.product(range(V), repeat=L):
+            t = rng.normal(0, 1.5, V)
+            if V > 2 and rng.random() < 0.3:
+                t[rng.integers(V)] = -np.inf
+            tgt[pre] = t.astype(np.float32)
+            if L < K:
+                d = t + rng.normal(0, 1.0, V)
+                d[~np.isfinite(d)] = rng.normal(0, 1.0)
+                if V > 2 and rng.random() < 0.3:
+                    d[rng.integers(V)] = -np.inf
+                if not np.isfinite(d).any():
+                    d[0] = 0.0
+                drf[pre] = d.astype(np.float32)
+    return tgt, drf
+
+
+def _probs(logits, T):
+    return torch.softmax(torch.from_numpy(logits.astype(np.float64)) / T, 0).numpy()
+
+
+def _cells(cuts):
+    pts = sorted(set([0.0, 1.0] + [c for c in cuts if 0.0 < c < 1.0]))
+    return [(a, b) for a, b in zip(pts[:-1], pts[1:]) if b > a]
+
+
+def _exact_joint(V, K, seed, T, variant):
+    """Joint law of the K+1 tokens obtained by one verify step followed by
+    plain target sampling of the remaining positions, integrated exactly over
+    the uniforms.  The uniforms' cells come from the breakpoints where any
+    correct sampler may change its answer; the oracle is probed at several
+    points per cell and must answer the same at all of them."""
+    tgt, drf = _tables(V, K, seed, T)
+    P = {k: _probs(v, T) for k, v in tgt.items()}
+    Q = {k: _probs(v, T) for k, v in drf.items()}
+    rows_t, rows_d, toks, us, meta = [], [], [], [], []
+    fracs = (0.13, 0.5, 0.87)
+    for x in itertools.product(range(V), repeat=K):
+        w = 1.0
+        for i in range(K):
+            w *= Q[x[:i]][x[i]]
+        if w == 0.0:
+            continue
+        # breakpoints of the accept tests
+        acc_cells = []
+        for i in range(K):
+            p, q = P[x[:i]][x[i]], Q[x[:i]][x[i]]
+            acc_cells.append(_cells([min(1.0, p / q)]))
+        # breakpoints of the final draw: CDF points of every row it may use
+        # (a superset of cuts is harmless: it only refines the cells)
+        cuts = []
+        for n in range(K + 1):
+            cuts.extend(np.cumsum(P[x[:n]]))
+            if n < K:
+                res = np.maximum(0.0, P[x[:n]] - Q[x[:n]])
+                if res.sum() > 0:
+                    cuts.extend(np.cumsum(res) / res.sum())
+        last_cells = _cells(cuts)
+        t_rows = np.stack([tgt[x[:i]] for i in range(K + 1)])
+        d_rows = np.stack([drf[x[:i]] for i in range(K)]) if K else np.zeros((0, V), np.float32)
+        for combo in itertools.product(*(acc_cells + [last_cells])):
+            m = w
+            for a, b in combo:
+                m *= b - a
+            if m == 0.0:
+                continue
+            for f in fracs:
+                u = np.array([a + f * (b - a) for a, b in combo], np.float32)
+                # keep the probe strictly inside its cell after fp32 rounding
+                u = np.array([min(max(v, np.nextafter(np.float32(a), np.float32(2))),
+                                  np.nextafter(np.float32(b), np.float32(-1)))
+                              for v, (a, b) in zip(u, combo)], np.float32)
+                rows_t.append(t_rows)
+                rows_d.append(d_rows)
+                toks.append(np.array(x, np.int32))
+                us.append(u)
+                meta.append((x, combo, m, f))
+    res = oracle.verify_ref(np.stack(rows_t), np.stack(rows_d), np.stack(toks).reshape(len(toks), K),
+                            np.stack(us), T, oracle.MODE_SAMPLE, variant)
+    assert res["status"] == 0
+    joint = np.zeros((V,) * (K + 1))
+    seen = {}
+    for j, (x, combo, m, f) in enumerate(meta):
+        n = int(res["accepted_len"][j])
+        emitted = tuple(int(v) for v in res["out_tokens"][j][: n + 1])
+        key = (x, combo)
+        if key in seen:
+            assert seen[key] == emitted, "oracle answer changes inside one cell"
+            continue
+        seen[key] = emitted
+        # finish the sequence with plain target sampling
+        for rest in itertools.product(range(V), repeat=K - n):
+            y = emitted + rest
+            pr = m
+            for k in range(n + 1, K + 1):
+                pr *= P[y[:k]][y[k]]
+            joint[y] += pr
+    target_joint = np.zeros_like(joint)
+    for y in itertools.product(range(V), repeat=K + 1):
+        pr = 1.0
+        for k in range(K + 1):
+            pr *= P[y[:k]][y[k]]
+        target_joint[y] = pr
+    return joint, target_joint
+
+
+@pytest.mark.parametrize("V,K,seed,T", [(2, 1, 1, 1.0), (3, 1, 2, 0.8), (3, 2, 3, 1.0),
+                                        (4, 2, 4, 1.3), (4, 1, 5, 0.7), (4, 2, 6, 1.0),
+                                        (3, 0, 7, 1.0)])
+def test_brute_force_output_law_is_the_target_law(V, K, seed, T):
+    joint, target = _exact_joint(V, K, seed, T, oracle.VARIANT_EXACT)
+    assert abs(joint.sum() - 1.0) < 1e-12
+    np.testing.assert_allclose(joint, target, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("V,K,seed", [(3, 1, 2), (4, 2, 4)])
+def test_brute_force_catches_literal_target_correction(V, K, seed):
+    """Negative control: drawing the correction from p_n (the literal wording
+    of the rejection-sampling page's step 4) is not exact."""
+    joint, target = _exact_joint(V, K, seed, 1.0, oracle.VARIANT_LITERAL_TARGET)
+    assert np.abs(joint - target).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# exactness by sampling: chi-square over 10^6 seeded trials, V = 8
+# --------------------------------------------------------------------------
+def _mc_batch(K, n_trials, seed, T=1.0):
+    V = 8
+    rng = np.random.default_rng(seed)
+    tgt, drf = {}, {}
+    for L in range(K + 1):
+        for pre in itertools.product(range(V), repeat=L):
+            t = rng.normal(0, 1.5, V).astype(np.float32)
+            tgt[pre] = t
+            if L < K:
+                drf[pre] = (t + rng.normal(0, 1.5, V)).astype(np.float32)
+    Q = {k: _probs(v, T) for k, v in drf.items()}
+    x = np.zeros((n_trials, K), np.int32)
+    for i in range(K):
+        for pre in itertools.product(range(V), repeat=i):
+            sel = np.all(x[:, :i] == np.array(pre, np.int32), axis=1) if i else np.ones(n_trials, bool)
+            cnt = int(sel.sum())
+            if cnt:
+                x[sel, i] = rng.choice(V, size=cnt, p=Q[pre])
+    t_rows = np.empty((n_trials, K + 1, V), np.float32)
+    d_rows = np.empty((n_trials, K, V), np.float32)
+    for i in range(K + 1):
+        for pre in itertools.product(range(V), repeat=i):
+            sel = np.all(x[:, :i] == np.array(pre, np.int32), axis=1) if i else np.ones(n_trials, bool)
+            t_rows[sel, i] = tgt[pre]
+            if i < K:
+                d_rows[sel, i] = drf[pre]
+    u = rng.random((n_trials, K + 1), dtype=np.float32)
+    return tgt, drf, t_rows, d_rows, x, u
+
+
+@pytest.mark.parametrize("K", [1, 2])
+def test_chi_square_first_token_follows_target(K):
+    n = 1_000_000
+    tgt, drf, t, d, x, u = _mc_batch(K, n, seed=11 + K)
+    res = oracle.verify_ref(t, d, x, u, 1.0)
+    first = res["out_tokens"][:, 0]
+    counts = np.bincount(first, minlength=8)
+    p0 = _probs(tgt[()], 1.0)
+    chi2, pval = stats.chisquare(counts, n * p0)
+    assert pval > 1e-3, (chi2, pval)
+    # negative control: the literal reading is rejected decisively
+    bad = oracle.verify_ref(t, d, x, u, 1.0, variant=oracle.VARIANT_LITERAL_TARGET)
+    counts_bad = np.bincount(bad["out_tokens"][:, 0], minlength=8)
+    _, pval_bad = stats.chisquare(counts_bad, n * p0)
+    assert pval_bad < 1e-12
+    # acceptance rate at position 0 is sum_x min(p, q)
+    q0 = _probs(drf[()], 1.0)
+    beta = np.minimum(p0, q0).sum()
+    acc = (res["accepted_len"] >= 1).mean()
+    assert abs(acc - beta) < 5 * np.sqrt(beta * (1 - beta) / n)
+
+
+def test_chi_square_second_token_given_first():
+    """K = 2: among trials whose first emitted token is a, the second emitted
+    token (when there is one, or the next target draw) follows p(. | a).
+    Trials that stopped at n = 0 are completed with a fresh target draw."""
+    n = 1_000_000
+    K = 2
+    tgt, drf, t, d, x, u = _mc_batch(K, n, seed=29)
+    res = oracle.verify_ref(t, d, x, u, 1.0)
+    out, nacc = res["out_tokens"], res["accepted_len"]
+    rng = np.random.default_rng(99)
+    second = out[:, 1].copy()
+    stop0 = nacc == 0
+    for a in range(8):
+        sel = stop0 & (out[:, 0] == a)
+        if sel.any():
+            second[sel] = rng.choice(8, size=int(sel.sum()), p=_probs(tgt[(a,)], 1.0))
+    for a in range(8):
+        sel = out[:, 0] == a
+        if sel.sum() < 2000:
+            continue
+        counts = np.bincount(second[sel], minlength=8)
+        pa = _probs(tgt[(a,)], 1.0)
+        _, pval = stats.chisquare(counts, sel.sum() * pa)
+        assert pval > 1e-4, (a, pval)
+
+
+# --------------------------------------------------------------------------
+# greedy: verification reproduces plain greedy decoding exactly
+# --------------------------------------------------------------------------
+def _toy_logits(prefix, V, seed, ties):
+    h = zlib.crc32(np.asarray(prefix, np.int64).tobytes()) ^ seed
+    r = np.random.default_rng(h)
+    if ties:
+        return r.integers(0, 4, V).astype(np.float32)  # many exact ties
+    return r.normal(0, 2, V).astype(np.float32)
+
+
+@pytest.mark.parametrize("V,K,ties,dtype", [(50, 4, False, "f32"), (17, 3, True, "f32"),
+                                            (64, 6, False, "bf16"), (9, 8, True, "bf16")])
+def test_greedy_verify_equals_plain_greedy_decoding(V, K, ties, dtype):
+    seed = V * 31 + K
+
+    def logits(prefix):
+        x = _toy_logits(prefix, V, seed, ties)
+        if dtype == "bf16":
+            return torch.from_numpy(x).to(torch.bfloat16)
+        return torch.from_numpy(x)
+
+    def raw(t):
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    ctx0 = [1, 2, 3]
+    m = 80
+    plain = list(ctx0)
+    while len(plain) < len(ctx0) + m:
+        plain.append(int(np.argmax(logits(plain).float().numpy())))
+    rng = np.random.default_rng(seed)
+    spec = list(ctx0)
+    calls = 0
+    while len(spec) < len(ctx0) + m:
+        # a noisy drafter: right most of the time, wrong sometimes
+        drafts, c = [], list(spec)
+        for _ in range(K):
+            g = int(np.argmax(logits(c).float().numpy()))
+            tok = g if rng.random() < 0.75 else int(rng.integers(V))
+            drafts.append(tok)
+            c.append(tok)
+        rows = np.stack([raw(logits(spec + drafts[:i])) for i in range(K + 1)])[None]
+        res = oracle.verify_ref(rows, None, np.array([drafts], np.int32), None,
+                                mode=oracle.MODE_GREEDY)
+        n = int(res["accepted_len"][0])
+        emitted = [int(v) for v in res["out_tokens"][0][: n + 1]]
+        assert (res["out_tokens"][0][n + 1:] == -1).all()
+        assert emitted[:n] == drafts[:n]
+        spec.extend(emitted)
+        calls += 1
+    assert spec[: len(plain)] == plain
+    assert calls < m  # more than one token per call on average
+
+
+def test_greedy_brute_force_all_draft_tuples():
+    """Every draft tuple at V = 4, K = 2, with tied maxima in the rows."""
+    V, K = 4, 2
+    rows = np.array([[1.0, 3.0, 3.0, 0.0], [2.0, 2.0, -np.inf, 1.0], [0.0, 0.0, 0.0, 0.0]],
+                    np.float32)
+    g = [1, 0, 0]  # lowest index among the maxima
+    xs = list(itertools.product(range(V), repeat=K))
+    t = np.stack([rows] * len(xs))
+    res = oracle.verify_ref(t, None, np.array(xs, np.int32), None, mode=oracle.MODE_GREEDY)
+    for j, x in enumerate(xs):
+        n = 0
+        while n < K and x[n] == g[n]:
+            n += 1
+        assert res["accepted_len"][j] == n
+        assert list(res["out_tokens"][j]) == list(x[:n]) + [g[n]] + [-1] * (K - n)
+
+
+# --------------------------------------------------------------------------
+# the worked examples printed on the pages
+# --------------------------------------------------------------------------
+def test_worked_example_in_the_bus():
+    fx = json.load(open(os.path.join(GOLDEN, "bpd_in_the_bus.json")))
+    vocab = fx["vocab"]
+    idx = {w: i for i, w in enumerate(vocab)}
+    rng = np.random.default_rng(0)
+    for case in fx["cases"]:
+        K = len(case["draft"])
+        rows = rng.normal(0, 0.5, (K + 1, len(vocab))).astype(np.float32)
+        for i, w in enumerate(case["target_top1"]):
+            rows[i, idx[w]] = 5.0
+        res = oracle.verify_ref(rows[None], None, np.array([[idx[w] for w in case["draft"]]], np.int32),
+                                None, mode=oracle.MODE_GREEDY)
+        assert res["accepted_len"][0] == case["expected_accepted_len"]
+        want = [-1 if w is None else idx[w] for w in case["expected_out"]]
+        assert list(res["out_tokens"][0]) == want
+
+
+def test_worked_example_quick_brown_fox():
+    fx = json.load(open(os.path.join(GOLDEN, "srs_quick_brown_fox.json")))
+    vocab = fx["vocab"]
+    idx = {w: i for i, w in enumerate(vocab)}
+    with np.errstate(divide="ignore"):
+        t = np.log(np.array(fx["target_probs"], np.float64)).astype(np.float32)
+        d = np.log(np.array(fx["draft_probs"], np.float64)).astype(np.float32)
+    x = np.array([[idx[w] for w in fx["draft"]]], np.int32)
+    u = np.array([fx["uniforms"]], np.float32)
+    res = oracle.verify_ref(t[None], d[None], x, u, fx["temperature"])
+    assert res["accepted_len"][0] == fx["expected_accepted_len"]
+    want = [-1 if w is None else idx[w] for w in fx["expected_out"]]
+    assert list(res["out_tokens"][0]) == want
+    # the outcome does not hinge on the chosen uniforms at positions 2 and K:
+    # 'brown' has no target mass and the residual is supported on 'fast' only
+    for u2 in (0.0, 0.999):
+        for uK in (0.0, 0.5, 0.9999):
+            uu = u.copy()
+            uu[0, 2], uu[0, 5] = u2, uK
+            r2 = oracle.verify_ref(t[None], d[None], x, uu, 1.0)
+            assert list(r2["out_tokens"][0]) == want
+
+
+# --------------------------------------------------------------------------
+# the accept rule's special cases and the first-rejection rule
+# --------------------------------------------------------------------------
+def _one(t, d, x, u, T=1.0):
+    return oracle.verify_ref(np.asarray(t, np.float32)[None], np.asarray(d, np.float32)[None],
+                             np.asarray(x, np.int32)[None], np.asarray(u, np.float32)[None], T,
+                             want_debug=True)
+
+
+def test_accept_when_target_at_least_draft_for_any_u():
+    u_max = np.nextafter(np.float32(1), np.float32(0))
+    t = [[2.0, 0.0, 0.0], [0.0, 0.0, 0.0]]   # p(0) > q(0)
+    d = [[1.0, 0.0, 0.0]]
+    for u0 in (0.0, 0.5, u_max):
+        r = _one(t, d, [0], [u0, 0.3])
+        assert r["accepted_len"][0] == 1
+
+
+def test_reject_when_target_has_no_mass_for_any_u():
+    t = [[-np.inf, 0.0, 0.0], [0.0, 0.0, 0.0]]
+    d = [[3.0, 0.0, 0.0]]
+    for u0 in (0.0, 1e-30, 0.5):
+        r = _one(t, d, [0], [u0, 0.3])
+        assert r["accepted_len"][0] == 0
+        assert r["out_tokens"][0][0] in (1, 2)   # never the zero-mass token
+
+
+def test_accept_when_draft_has_no_mass_but_target_does():
+    t = [[0.0, 0.0], [0.0, 0.0]]
+    d = [[-np.inf, 0.0]]
+    r = _one(t, d, [0], [0.999, 0.3])
+    assert r["accepted_len"][0] == 1
+
+
+def test_accept_probability_threshold_is_p_over_q():
+    # V = 2: p = (1/2, 1/2), q = (3/4, 1/4)  =>  p(0)/q(0) = 2/3
+    t = [[0.0, 0.0], [0.0, 0.0]]
+    d = [[np.log(3.0), 0.0]]
+    r = _one(t, d, [0], [0.6666, 0.3])
+    assert r["accepted_len"][0] == 1
+    r = _one(t, d, [0], [0.6668, 0.3])
+    assert r["accepted_len"][0] == 0
+    # the residual max(0, p - q) = (0, 1/4): token 1 for every u_K
+    for uK in (0.0, 0.5, 0.99):
+        r = _one(t, d, [0], [0.9, uK])
+        assert list(r["out_tokens"][0]) == [1, -1]
+
+
+def test_rows_after_first_rejection_do_not_matter():
+    rng = np.random.default_rng(5)
+    B, K, V = 200, 6, 30
+    t = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    d = (t[:, :K] + rng.normal(0, 2, (B, K, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    base = oracle.verify_ref(t, d, x, u)
+    n = base["accepted_len"]
+    assert ((n >= 0) & (n <= K)).all()
+    t2, d2, x2, u2 = t.copy(), d.copy(), x.copy(), u.copy()
+    for b in range(B):
+        if n[b] < K:
+            t2[b, n[b] + 1:] = rng.normal(0, 2, t2[b, n[b] + 1:].shape)
+            d2[b, n[b] + 1:] = rng.normal(0, 2, d2[b, n[b] + 1:].shape)
+            x2[b, n[b] + 1:] = rng.integers(0, V, K - n[b] - 1)
+            u2[b, n[b] + 1:K] = rng.random(K - n[b] - 1)
+    pert = oracle.verify_ref(t2, d2, x2, u2)
+    np.testing.assert_array_equal(pert["accepted_len"], n)
+    np.testing.assert_array_equal(pert["out_tokens"], base["out_tokens"])
+    assert (n < K).sum() > 50
+
+
+def test_identical_models_accept_everything_and_draw_the_bonus_from_p():
+    rng = np.random.default_rng(6)
+    B, K, V = 64, 5, 11
+    t = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    d = t[:, :K].copy()
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    r = oracle.verify_ref(t, d, x, u)
+    assert (r["accepted_len"] == K).all()
+    np.testing.assert_array_equal(r["out_tokens"][:, :K], x)
+    # V = 2 bonus row: token 0 iff u_K < p_K(0)
+    t2 = np.zeros((2, 2, 2), np.float32)
+    t2[:, 1] = [np.log(0.3), np.log(0.7)]
+    r2 = oracle.verify_ref(t2, t2[:, :1].copy(), np.zeros((2, 1), np.int32),
+                           np.array([[0.5, 0.2999], [0.5, 0.3001]], np.float32))
+    assert list(r2["out_tokens"][:, 1]) == [0, 1]
+
+
+def test_degenerate_shapes():
+    # K = 0: the step is a single draw from p_0
+    t = np.log(np.array([[[0.25, 0.75]]], np.float32))
+    r = oracle.verify_ref(t, np.zeros((1, 0, 2), np.float32), np.zeros((1, 0), np.int32),
+                          np.array([[0.2]], np.float32))
+    assert r["accepted_len"][0] == 0 and list(r["out_tokens"][0]) == [0]
+    # V = 1: p = q = 1, everything is accepted and the bonus is token 0
+    t1 = np.zeros((3, 4, 1), np.float32)
+    r = oracle.verify_ref(t1, t1[:, :3].copy(), np.zeros((3, 3), np.int32),
+                          np.full((3, 4), 0.99, np.float32))
+    assert (r["accepted_len"] == 3).all() and (r["out_tokens"] == 0).all()
+    # B = 0
+    r = oracle.verify_ref(np.zeros((0, 3, 5), np.float32), np.zeros((0, 2, 5), np.float32),
+                          np.zeros((0, 2), np.int32), np.zeros((0, 3), np.float32))
+    assert r["accepted_len"].shape == (0,)
+
+
+def test_data_errors_are_reported_per_sequence():
+    rng = np.random.default_rng(8)
+    B, K, V = 4, 2, 6
+    t = rng.normal(0, 1, (B, K + 1, V)).astype(np.float32)
+    d = rng.normal(0, 1, (B, K, V)).astype(np.float32)
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    x[1, 0] = V
+    t[2, 2, 3] = np.nan
+    u[3, 1] = 1.0
+    r = oracle.verify_ref(t, d, x, u)
+    assert r["status"] == oracle.DATA_TOKEN | oracle.DATA_LOGIT | oracle.DATA_UNIFORM
+    assert r["accepted_len"][0] >= 0
+    assert list(r["accepted_len"][1:]) == [-1, -1, -1]
+
+
+def test_boundary_flags_mark_uniforms_near_a_threshold():
+    t = [[0.0, 0.0], [0.0, 0.0]]
+    d = [[np.log(3.0), 0.0]]
+    r = _one(t, d, [0], [np.float32(2.0 / 3.0), 0.3])
+    assert r["flags"][0] & oracle.FLAG_RATIO
+    r = _one(t, d, [0], [0.2, 0.3])
+    assert r["flags"][0] == 0
+    # CDF boundary: accepted step, bonus row p = (0.5, 0.5), u_K at 0.5
+    t2 = [[0.0, 0.0], [0.0, 0.0]]
+    d2 = [[0.0, 0.0]]
+    r = _one(t2, d2, [0], [0.1, 0.5])
+    assert r["flags"][0] & oracle.FLAG_CDF
