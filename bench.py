@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark of the verify step (one JSON line on stdout).
+
+A step is one spec_verify call over one batch of the workload.  The default
+workload is the greedy blockwise-parallel verify of 64 sequences x 8 draft
+positions over a 32000-token bf16 vocabulary; ``--workload`` picks another of
+the seeded workloads (draft_verify_acceptance_gb300.workloads.WORKLOADS).
+
+Device timing: the inputs are resident in HBM as R rotating copies whose total
+exceeds twice the L2 size, so every step reads its logits from DRAM; K steps
+are captured in CUDA graphs and timed with CUDA events on the launching
+stream, bracketed by barrier + synchronize.  The metric is verified draft
+positions per second (B*K per step, summed over ranks) over the max time of
+all ranks.  ``e2e`` times the public call with pinned HOST tensors (copies
+host->device, the kernel, device->host of the outputs, per step).
+
+``--impl reference`` times the CPU oracle on the machine's host cores instead
+(rank 0 only) on the same workload and metric.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "greedy_bf16_B64_K8_V32000"
+METRIC = "verified draft positions/sec (B*K/s)"
+UNIT = "positions/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-workload table and the CPU baseline")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# --------------------------------------------------------------------------
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    """The largest value of x over all ranks (timing is taken as the max)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_seed(base_seed, rank):
+    """Each rank verifies its own independent batch (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thr = None
+
+    def _run(self):
+        try:
+            p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                  "--format=csv,noheader,nounits", "-lms", "100"],
+                                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        try:
+            for line in p.stdout:
+                self.samples.append((time.perf_counter(), line.strip()))
+                if self._stop.is_set():
+                    break
+        finally:
+            p.kill()
+            p.wait()
+
+    def start(self):
+        self._thr = threading.Thread(target=self._run, daemon=True)
+        self._thr.start()
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        self._stop.set()
+        self._thr.join(timeout=3)
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1] or [s for _, s in self.samples[-3:]]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# measured peaks and committed ncu traffic
+# --------------------------------------------------------------------------
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "draft_verify_acceptance_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, only if it was
+    taken on the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# native arm
+# --------------------------------------------------------------------------
+def device_time(binding, inp, steps, warmup, dev, l2_bytes):
+    """Prepare `steps` launches that rotate over R device copies of the inputs
+    (R * bytes > 2x L2), warm up, and capture them in CUDA graphs.  Returns
+    (R, algorithmic bytes per launch, stream, graphs to replay, two events)."""
+    import torch
+    nbytes = inp.algorithmic_bytes()
+    R = max(2, math.ceil(2 * l2_bytes / max(nbytes, 1)) + 1)
+    R = min(R, 64)
+    copies = []
+    for r in range(R):
+        copies.append(tuple(None if t is None else t.to(dev) for t in
+                            (inp.target, inp.draft, inp.tokens, inp.uniforms)))
+    acc = torch.empty(inp.B, dtype=torch.int32, device=dev)
+    out = torch.empty((inp.B, inp.K + 1), dtype=torch.int32, device=dev)
+    dt = binding.DTYPE_BF16 if inp.target.dtype == torch.bfloat16 else binding.DTYPE_F32
+    ws = torch.zeros(binding.workspace_size(inp.B, inp.K, inp.V, dt, inp.mode),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def launch(r):
+        c = copies[r % R]
+        binding.verify(c[0], c[1], c[2], c[3], inp.temperature, inp.mode, stream=stream,
+                       workspace=ws, out=(acc, out))
+
+    with torch.cuda.stream(stream):
+        for w in range(max(warmup, 3)):
+            launch(w)
+    stream.synchronize()
+    G = min(steps, 1000)
+    graphs = []
+    for n in sorted({G, steps % G} - {0}):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n):
+                launch(k)
+        graphs.append((n, g))
+    plan = [graphs[-1][1]] * (steps // G) if G else []
+    if steps % G:
+        plan.append([g for n, g in graphs if n == steps % G][0])
+    # one untimed replay of each graph
+    for _, g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    return R, nbytes, stream, plan, e0, e1
+
+
+def run_native(args, rank, world, local):
+    import torch
+    from draft_verify_acceptance_gb300 import binding, workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2**20)
+    inp = W.workload(args.workload, seed=shard_seed(0, rank))
+    R, nbytes, stream, plan, e0, e1 = device_time(binding, inp, args.steps, args.warmup, dev, l2)
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for g in plan:
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    barrier(world)
+    clk = clocks.stop(t0, t1) if rank == 0 else None
+    sec = e0.elapsed_time(e1) / 1e3
+    sec_max = max_over_ranks(sec, world)
+
+    positions = inp.B * inp.K
+    value = positions * world * args.steps / sec_max
+    per_launch = sec / args.steps
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / per_launch / 1e9
+
+    # end to end through the public call with pinned host tensors
+    e2e_steps = max(20, min(args.steps, 500))
+    host = [None if t is None else t.pin_memory() for t in
+            (inp.target, inp.draft, inp.tokens, inp.uniforms)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            binding.verify(*host, inp.temperature, inp.mode, stream=stream)
+        barrier(world)
+        h0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            binding.verify(*host, inp.temperature, inp.mode, stream=stream)
+        h1 = time.perf_counter()
+    e2e_sec = max_over_ranks(h1 - h0, world)
+    h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
+    d2h = inp.B * 4 + inp.B * (inp.K + 1) * 4
+
+    extras = None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_extras:
+        extras = per_workload_table(binding, args.workload, dev, l2, peak)
+        cpu = cpu_baseline(inp)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec_max * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded torch CPU generator; recipe in DESIGN.md)",
+        "config": {"workload": args.workload, "B": inp.B, "K": inp.K, "V": inp.V,
+                   "logits_dtype": inp.dtype_name,
+                   "mode": "greedy" if inp.mode == W.MODE_GREEDY else "sample",
+                   "temperature": inp.temperature if inp.mode == W.MODE_SAMPLE else None,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"{R} rotating input copies of {nbytes / 1e6:.1f} MB (> 2x L2 of "
+                         f"{l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA graphs of <=1000 launches, CUDA events on the launch stream"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": committed_traffic(args.workload),
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "kernel": "greedy_kernel" if inp.mode == W.MODE_GREEDY else "sample_kernel"},
+        "e2e": {"value": positions * world * e2e_steps / e2e_sec, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "binding.verify on pinned host tensors (H2D, kernel, D2H, sync)"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "workloads": extras,
+    }
+    print(json.dumps(line))
+
+
+def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
+    """Device throughput of every other workload (same timing method)."""
+    import torch
+    from draft_verify_acceptance_gb300 import workloads as W
+    table = {}
+    for name in W.WORKLOADS:
+        if name == skip:
+            continue
+        inp = W.workload(name)
+        R, nbytes, stream, plan, e0, e1 = device_time(binding, inp, steps, 5, dev, l2)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for g in plan:
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        sec = e0.elapsed_time(e1) / 1e3 / steps
+        table[name] = {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec,
+                       "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
+                       "algorithmic_bytes": nbytes}
+        del plan
+        torch.cuda.empty_cache()
+    return table
+
+
+def cpu_baseline(inp, budget_s=10.0):
+    """The oracle as it stands, on the host cores, over repetitions of the
+    workload's batch until about `budget_s` seconds have passed."""
+    import oracle
+    from draft_verify_acceptance_gb300 import workloads as W
+    t = W.as_numpy_logits(inp.target)
+    d = W.as_numpy_logits(inp.draft)
+    x = inp.tokens.numpy()
+    u = None if inp.uniforms is None else inp.uniforms.numpy()
+    B = inp.B
+    # a bounded sample: the first b sequences, doubled until one call takes >= 0.5 s
+    b = max(1, min(B, 4))
+    while True:
+        t0 = time.perf_counter()
+        oracle.verify_ref(t[:b], None if d is None else d[:b], x[:b], None if u is None else u[:b],
+                          inp.temperature, inp.mode)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 or b == B:
+            break
+        b = min(B, b * 2)
+    reps, total, t0 = 0, 0.0, time.perf_counter()
+    while total < budget_s:
+        oracle.verify_ref(t[:b], None if d is None else d[:b], x[:b], None if u is None else u[:b],
+                          inp.temperature, inp.mode)
+        reps += 1
+        total = time.perf_counter() - t0
+    return {"value": b * inp.K * reps / total, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"first {b} of {B} sequences, {reps} repetitions, {total:.1f} s"}
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# --------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from draft_verify_acceptance_gb300 import workloads as W
+    inp = W.workload(args.workload)
+    t = W.as_numpy_logits(inp.target)
+    d = W.as_numpy_logits(inp.draft)
+    x = inp.tokens.numpy()
+    u = None if inp.uniforms is None else inp.uniforms.numpy()
+
+    def step(b):
+        oracle.verify_ref(t[:b], None if d is None else d[:b], x[:b],
+                          None if u is None else u[:b], inp.temperature, inp.mode)
+
+    # each step: a bounded sample of the batch (<= ~0.2 s of CPU time)
+    b = 1
+    while b < inp.B:
+        t0 = time.perf_counter()
+        step(min(inp.B, b * 2))
+        if time.perf_counter() - t0 > 0.2:
+            break
+        b = min(inp.B, b * 2)
+    for _ in range(max(args.warmup, 1)):
+        step(b)
+    steps = args.steps if args.steps <= 2000 else 2000
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step(b)
+    sec = time.perf_counter() - t0
+    value = b * inp.K * steps / sec
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "B": inp.B, "K": inp.K,
+                                        "V": inp.V},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": f"first {b} of {inp.B} sequences per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_native(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,76 @@
+"""Build libspecverify.so (the C-ABI CUDA library) in-tree for sm_103a.
+
+Each translation unit under ``csrc/`` is compiled by nvcc in parallel, then
+linked into ``draft_verify_acceptance_gb300/libspecverify.so``.  Register and
+shared-memory usage reported by ptxas is written to ``_build/ptxas.log``.
+"""
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(HERE, "_build")
+LIB = os.path.join(HERE, "libspecverify.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+SOURCES = ["spec_verify.cu", "verify_greedy.cu", "verify_sample.cu"]
+
+
+def _nvcc():
+    exe = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(exe):
+        raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libspecverify.so")
+    return exe
+
+
+def _deps():
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(ROOT, "include", "spec_verify.h"))
+    files.append(os.path.abspath(__file__))
+    return files
+
+
+def _stale():
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    return any(os.path.getmtime(f) > t for f in _deps())
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link the library if any source is newer than it."""
+    if not force and not _stale():
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    nvcc = _nvcc()
+    common = [nvcc, "-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xptxas", "-v",
+              "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        r = subprocess.run(common + ["-c", os.path.join(CSRC, src), "-o", obj],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj, r.stderr
+
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+        for _, log in results:
+            f.write(log)
+    tmp = LIB + ".tmp"
+    r = subprocess.run([nvcc, "-shared", *ARCH, "-o", tmp] + [o for o, _ in results],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB)
+    if verbose:
+        print(open(os.path.join(BUILD, "ptxas.log")).read())
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force=True, verbose=True))

@@ -1,0 +1,152 @@
+// device_common.cuh -- loads, conversions and workspace layout shared by the
+// verify kernels (sm_103a).  Host-visible parts are plain structs.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace specv {
+
+constexpr int kThreads = 256;           // threads per CTA in every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCluster = 8;          // portable cluster size
+constexpr int kMaxTiles = 1024;         // tiles of kThreads vectors per CTA segment
+
+// Device status bits (same values as the public header's SPEC_DATA_*).
+constexpr int kDataTokenRange = 1;
+constexpr int kDataNonfiniteLogit = 2;
+constexpr int kDataUniformRange = 4;
+// Per-sequence boundary flags (public SPEC_FLAG_*).
+constexpr uint32_t kFlagRatio = 1;
+constexpr uint32_t kFlagCdf = 2;
+
+// Per-sequence state in the workspace.  Zero at rest: the kernel that
+// finalises a sequence puts every field back to zero.
+struct __align__(32) SeqState {
+  unsigned int arrivals;          // rows (sampling) or CTAs (greedy) done
+  unsigned int pad0;
+  unsigned long long reject_mask; // bit i: draft position i was rejected
+  unsigned long long near_mask;   // bit i: accept test i was within 1e-6
+  unsigned long long pad1;
+};
+static_assert(sizeof(SeqState) == 32, "SeqState layout");
+
+// Workspace: SeqState[B] followed by one 8-byte slot per row (B*(K+1)):
+// the candidate token of a sampled row (int32 in the low word, bit 31 = CDF
+// near-boundary) or the packed argmax key of a greedy row.
+inline size_t workspace_bytes(long long B, long long K) {
+  size_t n = (size_t)B * sizeof(SeqState) + (size_t)B * (size_t)(K + 1) * 8;
+  return (n + 255) & ~(size_t)255;
+}
+
+#ifdef __CUDACC__
+
+// ---- loads ---------------------------------------------------------------
+// 16-byte streaming load through the read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Element types: float (fp32) or the raw 16-bit pattern of a bf16.
+struct F32 {
+  using raw = float;
+  static constexpr int kBytes = 4;
+};
+struct BF16 {
+  using raw = uint16_t;
+  static constexpr int kBytes = 2;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// VEC consecutive elements starting at element v*VEC of `row`, as floats.
+// VEC is 16 bytes worth (4 fp32 / 8 bf16) for 16-byte aligned rows, else 1.
+template <typename E, int VEC>
+struct VecLoad;
+
+template <>
+struct VecLoad<F32, 4> {
+  static __device__ __forceinline__ void load(const void* row, long long v, float (&x)[4]) {
+    uint4 r = ld_stream_v4(static_cast<const float*>(row) + v * 4);
+    x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
+    x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
+  }
+};
+template <>
+struct VecLoad<BF16, 8> {
+  static __device__ __forceinline__ void load(const void* row, long long v, float (&x)[8]) {
+    uint4 r = ld_stream_v4(static_cast<const uint16_t*>(row) + v * 8);
+    x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x); x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
+    x[4] = bf16_lo(r.z); x[5] = bf16_hi(r.z); x[6] = bf16_lo(r.w); x[7] = bf16_hi(r.w);
+  }
+};
+template <>
+struct VecLoad<F32, 1> {
+  static __device__ __forceinline__ void load(const void* row, long long v, float (&x)[1]) {
+    x[0] = __ldg(static_cast<const float*>(row) + v);
+  }
+};
+template <>
+struct VecLoad<BF16, 1> {
+  static __device__ __forceinline__ void load(const void* row, long long v, float (&x)[1]) {
+    uint16_t h = __ldg(static_cast<const unsigned short*>(row) + v);
+    x[0] = __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+};
+
+// One element of a row, as float (for the gathers t[x], d[x]).
+template <typename E>
+__device__ __forceinline__ float load_one(const void* row, long long j);
+template <>
+__device__ __forceinline__ float load_one<F32>(const void* row, long long j) {
+  return __ldg(static_cast<const float*>(row) + j);
+}
+template <>
+__device__ __forceinline__ float load_one<BF16>(const void* row, long long j) {
+  uint16_t h = __ldg(static_cast<const unsigned short*>(row) + j);
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// ---- arithmetic ----------------------------------------------------------
+// 2^x on the SFU (PTX ex2.approx, flush-to-zero): 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Merge two partial softmax normalisers (m = max logit, z = sum 2^((x-m)s)).
+__device__ __forceinline__ void merge_mz(float& m, float& z, float m2, float z2, float s) {
+  float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) {  // both empty so far
+    m = mn;
+    z = 0.f;
+    return;
+  }
+  float a = (m == -INFINITY) ? 0.f : z * ex2((m - mn) * s);
+  float b = (m2 == -INFINITY) ? 0.f : z2 * ex2((m2 - mn) * s);
+  m = mn;
+  z = a + b;
+}
+
+// ---- workspace arrival ---------------------------------------------------
+// Make this thread's earlier global writes visible, then count one arrival
+// for sequence b.  Returns true for exactly one caller: the last of `total`.
+__device__ __forceinline__ bool arrive_last(SeqState* seq, int b, unsigned int total) {
+  __threadfence();
+  unsigned int prev = atomicAdd(&seq[b].arrivals, 1u);
+  if (prev + 1u == total) {
+    __threadfence();
+    return true;
+  }
+  return false;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace specv

@@ -1,0 +1,49 @@
+// launch.h -- internal host interface between the C ABI (spec_verify.cu)
+// and the kernel translation units.  Not part of the public API.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace specv {
+
+struct SeqState;
+
+// Everything a verify launch needs, already validated by the C ABI layer.
+struct VerifyArgs {
+  const void* target;          // [B, K+1, V]
+  const void* draft;           // [B, K, V] (sampling, K > 0)
+  const int32_t* tokens;       // [B, K]
+  const float* uniforms;       // [B, K+1] (sampling)
+  int B, K, V;
+  bool bf16;                   // element type of both logit tensors
+  bool vec;                    // rows are 16-byte aligned: 16-byte vector loads
+  float scale;                 // log2(e) / T (sampling)
+  int32_t* accepted_len;       // [B]
+  int32_t* out_tokens;         // [B, K+1]
+  float* p_at;                 // [B, K] or null
+  float* q_at;                 // [B, K] or null
+  uint32_t* flags;             // [B] or null
+  int32_t* status;             // device status word or null
+  SeqState* seq;               // workspace: [B]
+  void* slots;                 // workspace: [B*(K+1)] 8-byte slots
+};
+
+// Per-device facts gathered once.
+struct DeviceInfo {
+  int sm_count = 0;
+  int greedy_ctas_per_sm = 0;  // occupancy of the greedy kernel (vector path)
+};
+
+cudaError_t device_info(int device, DeviceInfo* out);
+
+// Launch configuration choices, exposed so the host logic can be tested.
+int greedy_segments(long long rows, long long nvec, int sm_count, int ctas_per_sm);
+int sample_cluster_size(long long V, int elem_bytes);
+long long sample_tiles(long long nvec, int cluster);
+
+cudaError_t launch_greedy(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace specv

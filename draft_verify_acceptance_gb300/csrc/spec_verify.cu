@@ -1,0 +1,147 @@
+// spec_verify.cu -- the C ABI of libspecverify.so (declared in
+// include/spec_verify.h): argument validation on the host, one-time per-
+// device set-up, and dispatch to the greedy or sampling kernel.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/spec_verify.h"
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace specv {
+
+cudaError_t greedy_occupancy(int* ctas_per_sm);
+cudaError_t sample_prepare();
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::once_flag g_once[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+cudaError_t g_err[kMaxDevices];
+}  // namespace
+
+// Gathered once per device, with that device current (the caller's).
+cudaError_t device_info(int device, DeviceInfo* out) {
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_once[device], [device]() {
+    DeviceInfo d;
+    cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = greedy_occupancy(&d.greedy_ctas_per_sm);
+    if (e == cudaSuccess) e = sample_prepare();
+    g_info[device] = d;
+    g_err[device] = e;
+  });
+  *out = g_info[device];
+  return g_err[device];
+}
+
+}  // namespace specv
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int B, int K, int V, int dtype, int mode) {
+  if (B < 0 || K < 0 || K > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return 0;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return 0;
+  if (mode != SPEC_MODE_SAMPLE && mode != SPEC_MODE_GREEDY) return 0;
+  return specv::workspace_bytes(B, K);
+}
+
+spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits,
+                             const int32_t* draft_tokens, const float* uniforms, int B,
+                             int K, int V, int dtype, float temperature, int mode,
+                             int32_t* accepted_len, int32_t* out_tokens, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream,
+                             float* p_at_draft, float* q_at_draft, uint32_t* flags,
+                             int32_t* device_status) {
+  // ---- sizes, enums ------------------------------------------------------
+  if (B < 0 || K < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (mode != SPEC_MODE_SAMPLE && mode != SPEC_MODE_GREEDY) return SPEC_ERR_INVALID_ARG;
+  if (K > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
+  const bool sample = mode == SPEC_MODE_SAMPLE;
+  if (sample && !(temperature > 0.f && std::isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+
+  // ---- pointers ----------------------------------------------------------
+  const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  if (!target_logits || !aligned(target_logits, esz)) return SPEC_ERR_INVALID_ARG;
+  if (K > 0 && (!draft_tokens || !aligned(draft_tokens, 4))) return SPEC_ERR_INVALID_ARG;
+  if (!accepted_len || !aligned(accepted_len, 4)) return SPEC_ERR_INVALID_ARG;
+  if (!out_tokens || !aligned(out_tokens, 4)) return SPEC_ERR_INVALID_ARG;
+  if (sample) {
+    if (K > 0 && (!draft_logits || !aligned(draft_logits, esz))) return SPEC_ERR_INVALID_ARG;
+    if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_INVALID_ARG;
+  }
+  if ((p_at_draft && !aligned(p_at_draft, 4)) || (q_at_draft && !aligned(q_at_draft, 4)) ||
+      (flags && !aligned(flags, 4)) || (device_status && !aligned(device_status, 4)))
+    return SPEC_ERR_INVALID_ARG;
+  const size_t need = specv::workspace_bytes(B, K);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return SPEC_ERR_INVALID_ARG;
+
+  // ---- launch ------------------------------------------------------------
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  specv::DeviceInfo info;
+  if (specv::device_info(dev, &info) != cudaSuccess) return SPEC_ERR_CUDA;
+
+  specv::VerifyArgs a;
+  a.target = target_logits;
+  a.draft = (sample && K > 0) ? draft_logits : nullptr;
+  a.tokens = draft_tokens;
+  a.uniforms = sample ? uniforms : nullptr;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.bf16 = dtype == SPEC_DTYPE_BF16;
+  const long long rowbytes = static_cast<long long>(V) * esz;
+  a.vec = (rowbytes % 16 == 0) && aligned(target_logits, 16) && (!a.draft || aligned(a.draft, 16));
+  a.scale = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 0.f;
+  a.accepted_len = accepted_len;
+  a.out_tokens = out_tokens;
+  a.p_at = sample ? p_at_draft : nullptr;
+  a.q_at = sample ? q_at_draft : nullptr;
+  a.flags = flags;
+  a.status = device_status;
+  a.seq = static_cast<specv::SeqState*>(workspace);
+  a.slots = static_cast<char*>(workspace) + static_cast<size_t>(B) * sizeof(specv::SeqState);
+
+  const long long rows = static_cast<long long>(B) * (K + 1);
+  if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
+  if (sample) {
+    const long long nvec = a.vec ? rowbytes / 16 : V;
+    const int C = specv::sample_cluster_size(V, esz);
+    if (specv::sample_tiles(nvec, C) > specv::kMaxTiles) return SPEC_ERR_UNSUPPORTED;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = sample ? specv::launch_sample(a, info, s) : specv::launch_greedy(a, info, s);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
+                          const int32_t* draft_tokens, const float* uniforms, int B, int K,
+                          int V, int dtype, float temperature, int mode,
+                          int32_t* accepted_len, int32_t* out_tokens, void* workspace,
+                          size_t workspace_bytes, spec_stream_t stream) {
+  return spec_verify_ex(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype,
+                        temperature, mode, accepted_len, out_tokens, workspace,
+                        workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr);
+}
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported size";
+    case SPEC_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+// verify_greedy.cu -- greedy (blockwise-parallel) verification on sm_103a.
+//
+// "Garden | Blockwise Parallel Decoding", sections 3.2 (Accept) and 3.5:
+// the target's argmax g_i at each of the K+1 positions is compared with the
+// draft token x_i; the longest matching prefix is kept and the target's own
+// token g_n is emitted at the first mismatch n (or at K when all match).
+//
+// Design: the [B*(K+1), V] logit rows are streamed once from HBM with 16-byte
+// non-allocating loads.  Each row is split into S segments, one CTA each, so
+// that the whole grid is resident in about one wave; a CTA reduces its
+// segment to (max value, lowest index) and folds it into the row's packed
+// 64-bit key with one atomicMax.  The CTA that arrives last for a sequence
+// (a counter in the workspace, no waiting) compares the K+1 argmaxes with
+// the draft tokens, writes the outputs and puts the workspace back to zero.
+#include <cfloat>
+#include <climits>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace specv {
+
+namespace {
+
+// Total order on floats for atomicMax: larger float -> larger key; -0 == +0.
+__device__ __forceinline__ unsigned int orderable(float f) {
+  unsigned int u = __float_as_uint(__fadd_rn(f, 0.0f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Larger key wins: higher value first, then the LOWER index.
+__device__ __forceinline__ unsigned long long pack_key(float v, int idx) {
+  return (static_cast<unsigned long long>(orderable(v)) << 32) |
+         static_cast<unsigned long long>(0xffffffffu - static_cast<unsigned int>(idx));
+}
+
+__device__ __forceinline__ int key_index(unsigned long long key) {
+  return static_cast<int>(0xffffffffu - static_cast<unsigned int>(key & 0xffffffffull));
+}
+
+__device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+template <typename E, int VEC, int U>
+__global__ void __launch_bounds__(kThreads)
+greedy_kernel(VerifyArgs a, long long nvec, int S) {
+  const int K1 = a.K + 1;
+  const long long row = blockIdx.x / S;
+  const int seg = static_cast<int>(blockIdx.x - row * S);
+  const int b = static_cast<int>(row / K1);
+  const long long v0 = nvec * seg / S;
+  const long long v1 = nvec * (seg + 1) / S;
+  const char* base = static_cast<const char*>(a.target) +
+                     static_cast<size_t>(row) * static_cast<size_t>(a.V) * E::kBytes;
+
+  const int tid = threadIdx.x;
+  float best = -INFINITY;
+  int bidx = (v0 + tid < v1) ? static_cast<int>((v0 + tid) * VEC) : INT_MAX;
+  bool bad = false;
+
+  for (long long v = v0 + tid; v < v1; v += static_cast<long long>(kThreads) * U) {
+    float x[U][VEC];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long vv = v + static_cast<long long>(u) * kThreads;
+      if (vv < v1) {
+        VecLoad<E, VEC>::load(base, vv, x[u]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) x[u][k] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int k = 0; k < VEC; ++k) {
+        const float e = x[u][k];
+        bad |= !(e <= FLT_MAX);  // NaN or +inf
+        if (e > best) {
+          best = e;
+          bidx = static_cast<int>((v + static_cast<long long>(u) * kThreads) * VEC + k);
+        }
+      }
+    }
+  }
+
+  // block argmax: warp butterfly, then across warps in a fixed order
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, bidx, off);
+    argmax_merge(best, bidx, ov, oi);
+  }
+  __shared__ float s_v[kWarps];
+  __shared__ int s_i[kWarps];
+  const int warp = tid >> 5, lane = tid & 31;
+  if (lane == 0) {
+    s_v[warp] = best;
+    s_i[warp] = bidx;
+  }
+  const int any_bad = __syncthreads_or(bad);
+  if (tid != 0) return;
+
+  for (int w = 1; w < kWarps; ++w) argmax_merge(best, bidx, s_v[w], s_i[w]);
+  if (any_bad && a.status) atomicOr(a.status, kDataNonfiniteLogit);
+
+  unsigned long long* keys = static_cast<unsigned long long*>(a.slots);
+  const unsigned long long key = pack_key(best, bidx);
+  if (S == 1) keys[row] = key;
+  else atomicMax(&keys[row], key);
+
+  if (!arrive_last(a.seq, b, static_cast<unsigned int>(K1) * static_cast<unsigned int>(S)))
+    return;
+
+  // last arrival for sequence b: longest matching prefix, outputs, reset
+  volatile unsigned long long* vkeys = keys + static_cast<size_t>(b) * K1;
+  const int32_t* x = a.tokens + static_cast<size_t>(b) * a.K;
+  int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
+  int n = a.K;
+  bool bad_tok = false;
+  for (int i = 0; i < a.K; ++i) {
+    const int xi = x[i];
+    bad_tok |= (xi < 0 || xi >= a.V);
+    if (n == a.K && xi != key_index(vkeys[i])) n = i;
+  }
+  for (int i = 0; i < n; ++i) out[i] = x[i];
+  out[n] = key_index(vkeys[n]);
+  for (int i = n + 1; i < K1; ++i) out[i] = -1;
+  a.accepted_len[b] = n;
+  if (a.flags) a.flags[b] = 0;
+  if (bad_tok && a.status) atomicOr(a.status, kDataTokenRange);
+  for (int i = 0; i < K1; ++i) vkeys[i] = 0ull;
+  a.seq[b].arrivals = 0u;
+}
+
+template <typename E, int VEC, int U>
+cudaError_t launch_greedy_t(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  const long long nvec = a.V / VEC;
+  const long long rows = static_cast<long long>(a.B) * (a.K + 1);
+  const int S = greedy_segments(rows, nvec, dev.sm_count, dev.greedy_ctas_per_sm);
+  const long long grid = rows * S;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned int>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, greedy_kernel<E, VEC, U>, a, nvec, S);
+}
+
+}  // namespace
+
+// Segments per row: enough CTAs to fill every SM once (one resident wave),
+// but never fewer than ~2 loads of 16 bytes per thread in a segment.
+int greedy_segments(long long rows, long long nvec, int sm_count, int ctas_per_sm) {
+  if (rows <= 0 || nvec <= 0) return 1;
+  const long long slots = static_cast<long long>(sm_count > 0 ? sm_count : 1) *
+                          (ctas_per_sm > 0 ? ctas_per_sm : 1);
+  long long S = slots / rows;
+  const long long max_s = nvec / (2LL * kThreads);
+  if (S > max_s) S = max_s;
+  if (S < 1) S = 1;
+  if (S > 64) S = 64;
+  return static_cast<int>(S);
+}
+
+cudaError_t greedy_occupancy(int* ctas_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm,
+                                                       greedy_kernel<BF16, 8, 4>, kThreads, 0);
+}
+
+cudaError_t launch_greedy(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  if (a.bf16) {
+    return a.vec ? launch_greedy_t<BF16, 8, 4>(a, dev, stream)
+                 : launch_greedy_t<BF16, 1, 8>(a, dev, stream);
+  }
+  return a.vec ? launch_greedy_t<F32, 4, 4>(a, dev, stream)
+               : launch_greedy_t<F32, 1, 8>(a, dev, stream);
+}
+
+}  // namespace specv

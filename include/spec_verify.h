@@ -1,0 +1,162 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) draft-then-verify acceptance
+ * step of speculative decoding.  Library: libspecverify.so.
+ *
+ * The operation (sources named by page title and section):
+ *   - "推测性拒绝采样" (speculative rejection sampling), section 技术原理与步骤:
+ *     step 2, the target scores every draft prefix in one parallel pass, so
+ *     its logits exist at K+1 positions; step 3, each draft token x_i is
+ *     accepted when p(x_i) >= q(x_i) and otherwise with probability
+ *     p(x_i)/q(x_i), and everything after the first rejection is dropped;
+ *     step 4, one replacement token is drawn at the rejected position.
+ *     Section 关键保证 states that the emitted tokens follow the target's own
+ *     distribution exactly, which fixes the replacement law to the
+ *     normalised residual max(0, p - q).
+ *   - "논문 리뷰 [Speculative Contrastive Decoding]", section Speculative
+ *     Decoding: when all K draft tokens are accepted the target adds token
+ *     K+1 (the bonus token, drawn from p at position K).
+ *   - "Garden | Blockwise Parallel Decoding", sections 3.2 and 3.5: greedy
+ *     verification keeps the longest prefix on which the draft equals the
+ *     target's argmax and emits the target's argmax at the first mismatch.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are row-major and contiguous.  Device pointers refer to
+ *     memory of the current CUDA device.  The caller owns every buffer; the
+ *     library allocates nothing and keeps no state between calls except a
+ *     one-time per-device kernel attribute set-up on first use.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are detected on the host before anything is launched
+ *     and nothing is written then.  Errors in the data (see SPEC_DATA_*) are
+ *     reported through an optional device status word, readable after the
+ *     stream has been synchronised.
+ *   - No entry point traps, aborts, prints, or waits on the device.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t / CUstream). */
+typedef struct CUstream_st* spec_stream_t;
+
+/* Return codes. */
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,  /* bad pointer, size, dtype, mode, temperature or workspace */
+  SPEC_ERR_UNSUPPORTED = 2,  /* valid request beyond this build's limits (K, V, grid) */
+  SPEC_ERR_CUDA = 3          /* a CUDA runtime call or launch failed */
+} spec_status_t;
+
+typedef enum { SPEC_MODE_SAMPLE = 0, SPEC_MODE_GREEDY = 1 } spec_mode_t;
+typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
+
+/* Build limits. */
+#define SPEC_MAX_K 64          /* draft positions per sequence */
+#define SPEC_MAX_V (1 << 22)   /* vocabulary size */
+
+/* Device status bits (OR-ed into *device_status by the kernels).  A sequence
+ * with a data error gets outputs that are in range but otherwise unspecified. */
+#define SPEC_DATA_TOKEN_RANGE 1      /* a draft token outside [0, V) (clamped) */
+#define SPEC_DATA_NONFINITE_LOGIT 2  /* NaN or +inf logit, or a row with no finite entry */
+#define SPEC_DATA_UNIFORM_RANGE 4    /* a uniform outside [0, 1) or NaN */
+
+/* Per-sequence boundary flags (sampling mode; written when `flags` is given).
+ * They mark decisions the kernel took within 1e-6 of a threshold, where a
+ * different rounding order could legitimately decide the other way. */
+#define SPEC_FLAG_RATIO 1  /* |u_i - min(1, p/q)| < 1e-6 at an evaluated position i <= n */
+#define SPEC_FLAG_CDF 2    /* u_K within 1e-6 (relative to the mass) of a CDF step */
+
+/*
+ * Bytes of workspace a call with these sizes needs (a multiple of 256).
+ * The workspace holds per-sequence arrival counters, reject masks and
+ * per-row candidates.  It MUST be zero-filled before its first use; every
+ * call that returns SPEC_OK leaves it zero-filled again when the kernel
+ * completes, so it can be reused by later calls on the same stream without
+ * clearing.  One workspace serves one call at a time: calls that may overlap
+ * on the GPU need separate workspaces.  Returns 0 for invalid sizes.
+ */
+SPEC_API size_t spec_verify_workspace_size(int B, int K, int V, int dtype, int mode);
+
+/*
+ * spec_verify -- one verify step for B independent sequences.
+ *
+ *   target_logits [B, K+1, V]  dtype, device.  Row (b, i) holds the target's
+ *                              logits after prefix x_{<i}; row K is the bonus
+ *                              position.
+ *   draft_logits  [B, K, V]    dtype, device.  Row (b, i) holds the draft's
+ *                              logits that x_i was sampled from.  Unused (may
+ *                              be NULL) in greedy mode or when K == 0.
+ *   draft_tokens  [B, K]       int32 in [0, V), device.  May be NULL if K == 0.
+ *   uniforms      [B, K+1]     fp32 in [0, 1), device.  u_i (i < K) drives the
+ *                              accept test of position i; u_K is the single
+ *                              uniform of the replacement / bonus draw.
+ *                              Unused (may be NULL) in greedy mode.
+ *   B, K, V                    B >= 0 (B == 0 is a no-op), 0 <= K <= SPEC_MAX_K,
+ *                              1 <= V <= SPEC_MAX_V.
+ *   dtype                      SPEC_DTYPE_F32 or SPEC_DTYPE_BF16 (both logits).
+ *   temperature                > 0 and finite in sampling mode: p = softmax(t/T),
+ *                              q = softmax(d/T).  Ignored in greedy mode.
+ *   mode                       SPEC_MODE_SAMPLE or SPEC_MODE_GREEDY.
+ *   accepted_len  [B]          int32 out, device: n = number of accepted draft
+ *                              tokens, in [0, K].
+ *   out_tokens    [B, K+1]     int32 out, device: x_0..x_{n-1}, then the
+ *                              replacement (n < K) or bonus (n == K) token,
+ *                              then -1 padding.
+ *   workspace, workspace_bytes caller-owned device memory, at least
+ *                              spec_verify_workspace_size(...) bytes, 16-byte
+ *                              aligned, zero-filled before first use (above).
+ *   stream                     CUDA stream the work is queued on.
+ *
+ * Sampling mode:  accept x_i iff u_i * q_i(x_i) < p_i(x_i); n = first rejected
+ * position (K if none); at n < K the replacement is the smallest token j
+ * with C_j > u_K * S, C the inclusive running sum in token order of
+ * max(0, p_n - q_n) and S its total (p_n itself if S == 0); at n == K the
+ * same inverse CDF is taken on p_K.
+ * Greedy mode:  g_i = argmax_j t[b, i, j] compared as fp32 values, lowest index
+ * on ties; n = first i < K with x_i != g_i (K if none); the emitted token at n
+ * is g_n.
+ *
+ * Returns SPEC_OK once the work is queued, or an error code (nothing queued).
+ */
+SPEC_API spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
+                          const int32_t* draft_tokens, const float* uniforms, int B, int K,
+                          int V, int dtype, float temperature, int mode,
+                          int32_t* accepted_len, int32_t* out_tokens, void* workspace,
+                          size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_verify_ex -- spec_verify plus optional diagnostics (each may be NULL):
+ *   p_at_draft    [B, K] fp32 out, device: p_i(x_i) for every position
+ *   q_at_draft    [B, K] fp32 out, device: q_i(x_i) for every position
+ *                 (both sampling mode only; left untouched in greedy mode)
+ *   flags         [B] uint32 out, device: SPEC_FLAG_* bits (0 in greedy mode)
+ *   device_status int32 in/out, device: the kernels OR SPEC_DATA_* bits into
+ *                 it.  The caller zeroes it; it is not cleared by the library.
+ */
+SPEC_API spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits,
+                             const int32_t* draft_tokens, const float* uniforms, int B,
+                             int K, int V, int dtype, float temperature, int mode,
+                             int32_t* accepted_len, int32_t* out_tokens, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream,
+                             float* p_at_draft, float* q_at_draft, uint32_t* flags,
+                             int32_t* device_status);
+
+/* A short, static, human-readable description of a return code. */
+SPEC_API const char* spec_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

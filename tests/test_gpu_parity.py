@@ -1,0 +1,269 @@
+"""Parity of the CUDA verify path (through the C ABI) with the CPU oracle.
+
+Bar (per sequence):
+  greedy   accepted_len and out_tokens bit-equal, always;
+  sampling accepted_len and out_tokens bit-equal for every sequence the
+           oracle does not flag as a boundary case (a uniform within 1e-6 of
+           an accept ratio or of a CDF step, or a residual mass below 1e-6);
+           flagged sequences are counted and must still be valid outputs;
+  p_i(x_i), q_i(x_i) within 1e-5 absolute (fp32 logits) or 2e-3 (bf16);
+  the device status word equals the oracle's data-error bits.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from draft_verify_acceptance_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    from draft_verify_acceptance_gb300 import binding
+    return binding
+
+
+def _dev(t):
+    return None if t is None else t.to("cuda")
+
+
+def run_gpu(lib, inp, **kw):
+    res = lib.verify_ex(_dev(inp.target), _dev(inp.draft), _dev(inp.tokens), _dev(inp.uniforms),
+                        inp.temperature, inp.mode, **kw)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def run_oracle(inp):
+    return oracle.verify_ref(W.as_numpy_logits(inp.target), W.as_numpy_logits(inp.draft),
+                             inp.tokens.numpy(),
+                             None if inp.uniforms is None else inp.uniforms.numpy(),
+                             inp.temperature, inp.mode, want_debug=True)
+
+
+def check_valid(g, inp):
+    n, out, x = g["accepted_len"], g["out_tokens"], inp.tokens.numpy()
+    K = inp.K
+    assert ((n >= 0) & (n <= K)).all()
+    for b in range(inp.B):
+        nb = int(n[b])
+        assert (out[b, :nb] == x[b, :nb]).all()
+        assert 0 <= out[b, nb] < inp.V
+        assert (out[b, nb + 1:] == -1).all()
+
+
+def assert_parity(g, ref, inp, label=""):
+    status = int(g["status"][0])
+    assert status == ref["status"], (label, status, ref["status"])
+    if status:
+        return {"flagged": 0, "B": inp.B}
+    check_valid(g, inp)
+    if inp.mode == W.MODE_GREEDY:
+        np.testing.assert_array_equal(g["accepted_len"], ref["accepted_len"], err_msg=label)
+        np.testing.assert_array_equal(g["out_tokens"], ref["out_tokens"], err_msg=label)
+        return {"flagged": 0, "B": inp.B}
+    flagged = ref["flags"] != 0
+    bad = (g["accepted_len"] != ref["accepted_len"]) | (g["out_tokens"] != ref["out_tokens"]).any(1)
+    unflagged_bad = np.nonzero(bad & ~flagged)[0]
+    if len(unflagged_bad):
+        b = int(unflagged_bad[0])
+        pytest.fail(f"{label}: {len(unflagged_bad)} unflagged mismatches; first b={b} "
+                    f"gpu n={g['accepted_len'][b]} out={g['out_tokens'][b].tolist()} "
+                    f"oracle n={ref['accepted_len'][b]} out={ref['out_tokens'][b].tolist()} "
+                    f"u={inp.uniforms[b].tolist()} p={ref['p_at'][b].tolist()} "
+                    f"q={ref['q_at'][b].tolist()} gpu_flags={g['flags'][b]}")
+    tol = 1e-5 if inp.target.dtype == torch.float32 else 2e-3
+    if inp.K:
+        dp = np.abs(g["p_at"] - ref["p_at"]).max()
+        dq = np.abs(g["q_at"] - ref["q_at"]).max()
+        assert dp <= tol and dq <= tol, (label, dp, dq)
+    print(f"{label}: {inp.B - int(flagged.sum())}/{inp.B} bit-equal, "
+          f"{int(flagged.sum())} boundary-flagged ({int((bad & flagged).sum())} of them differ)")
+    return {"flagged": int(flagged.sum()), "B": inp.B}
+
+
+SAMPLE_CASES = [
+    # name, B, K, V, dtype, T, recipe
+    ("f32_V1000", 16, 4, 1000, torch.float32, 1.0, dict(target_std=3.0, draft_noise=0.5)),
+    ("bf16_V7_scalar", 8, 5, 7, torch.bfloat16, 1.0, dict(target_std=2.0, draft_noise=1.0)),
+    ("f32_V33_scalar", 8, 3, 33, torch.float32, 0.9, dict(target_std=2.0, draft_noise=1.0)),
+    ("f32_V20000_C3", 6, 6, 20000, torch.float32, 0.8, dict(target_std=5.0, independent_draft=True)),
+    ("bf16_V70001_C5_scalar", 6, 5, 70001, torch.bfloat16, 1.0,
+     dict(target_std=4.0, zipf_s=1.1, draft_noise=1.0)),
+    ("bf16_V128256_C8", 4, 5, 128256, torch.bfloat16, 0.7,
+     dict(target_std=4.0, zipf_s=1.1, draft_noise=1.0)),
+    ("f32_V152064_C8", 3, 16, 152064, torch.float32, 0.8, dict(target_std=5.0, independent_draft=True)),
+    ("bf16_V32000_high_accept", 32, 4, 32000, torch.bfloat16, 1.0, dict(target_std=3.0, draft_noise=0.3)),
+    ("f32_K0", 6, 0, 5000, torch.float32, 1.0, dict(target_std=3.0)),
+    ("f32_Kmax", 3, 64, 300, torch.float32, 1.0, dict(target_std=1.0, draft_noise=0.2)),
+    ("f32_V1", 5, 3, 1, torch.float32, 1.0, dict(target_std=1.0)),
+    ("f32_V2", 64, 3, 2, torch.float32, 1.0, dict(target_std=1.0, draft_noise=1.0)),
+    ("bf16_V3", 64, 2, 3, torch.bfloat16, 1.5, dict(target_std=1.0, draft_noise=1.0)),
+    ("bf16_V4096_T0.05", 16, 4, 4096, torch.bfloat16, 0.05, dict(target_std=1.0, draft_noise=0.1)),
+]
+
+
+@pytest.mark.parametrize("name,B,K,V,dtype,T,recipe", SAMPLE_CASES, ids=[c[0] for c in SAMPLE_CASES])
+def test_sampling_parity(lib, name, B, K, V, dtype, T, recipe):
+    inp = W.make_inputs(B, K, V, dtype=dtype, temperature=T, seed=zlib.crc32(name.encode()) % 1000, name=name,
+                        **recipe)
+    assert_parity(run_gpu(lib, inp), run_oracle(inp), inp, name)
+
+
+GREEDY_CASES = [
+    ("bf16_V32000", 64, 8, 32000, torch.bfloat16, dict(target_std=4.0)),
+    ("f32_V1000", 16, 5, 1000, torch.float32, dict(target_std=2.0, greedy_noise=0.5)),
+    ("bf16_V7_scalar", 12, 5, 7, torch.bfloat16, dict(target_std=1.0, greedy_noise=0.3)),
+    ("f32_V152064", 4, 3, 152064, torch.float32, dict(target_std=5.0, greedy_noise=0.1)),
+    ("bf16_K0", 8, 0, 2000, torch.bfloat16, dict(target_std=3.0)),
+    ("f32_Kmax", 3, 64, 200, torch.float32, dict(target_std=3.0, greedy_noise=0.01)),
+    ("f32_V1", 4, 2, 1, torch.float32, dict()),
+]
+
+
+@pytest.mark.parametrize("name,B,K,V,dtype,recipe", GREEDY_CASES, ids=[c[0] for c in GREEDY_CASES])
+def test_greedy_parity(lib, name, B, K, V, dtype, recipe):
+    inp = W.make_inputs(B, K, V, dtype=dtype, mode=W.MODE_GREEDY, seed=zlib.crc32(name.encode()) % 1000,
+                        name=name, **recipe)
+    assert_parity(run_gpu(lib, inp), run_oracle(inp), inp, name)
+
+
+def test_greedy_ties_take_the_lowest_index(lib):
+    """Integer-valued bf16 logits: most rows have tied maxima, some across
+    the split of a row into segments."""
+    g = torch.Generator().manual_seed(5)
+    B, K, V = 32, 6, 40000
+    t = torch.randint(0, 3, (B, K + 1, V), generator=g).to(torch.bfloat16)
+    t[:, :, -1] = 2.0          # a tie at the very end of every row
+    t[0, :, :] = 0.0           # fully tied rows
+    t[1, :, :] = float("-inf")
+    x = t[:, :K].float().argmax(-1).to(torch.int32)
+    x[::3, 2] = 7              # some mismatches
+    inp = W.Inputs("ties", W.MODE_GREEDY, B, K, V, 1.0, t.contiguous(), None, x.contiguous(), None)
+    assert_parity(run_gpu(lib, inp), run_oracle(inp), inp, "ties")
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_full_size_workloads(lib, name):
+    inp = W.workload(name)
+    assert_parity(run_gpu(lib, inp), run_oracle(inp), inp, name)
+
+
+def test_maximum_vocabulary(lib):
+    V = lib.MAX_V
+    inp = W.make_inputs(1, 1, V, dtype=torch.float32, temperature=1.0, target_std=3.0,
+                        draft_noise=1.0, seed=4, name="maxV")
+    assert_parity(run_gpu(lib, inp), run_oracle(inp), inp, "maxV")
+
+
+def test_identical_models_accept_everything(lib):
+    inp = W.make_inputs(16, 5, 3000, dtype=torch.bfloat16, seed=9, name="same")
+    inp.draft = inp.target[:, :5].clone()
+    inp.tokens = torch.randint(0, 3000, (16, 5), dtype=torch.int32)
+    g, ref = run_gpu(lib, inp), run_oracle(inp)
+    assert (g["accepted_len"] == 5).all()
+    assert_parity(g, ref, inp, "same")
+
+
+def test_neg_inf_logits_are_allowed(lib):
+    inp = W.make_inputs(8, 4, 2000, dtype=torch.float32, seed=10, name="neginf")
+    inp.target[:, :, ::3] = float("-inf")
+    inp.draft[:, :, 1::3] = float("-inf")
+    g, ref = run_gpu(lib, inp), run_oracle(inp)
+    assert int(g["status"][0]) == 0
+    assert_parity(g, ref, inp, "neginf")
+    zero = inp.target.numpy()[np.arange(8)[:, None], np.arange(5)[None], g["out_tokens"].clip(0)]
+    emitted = g["out_tokens"] >= 0
+    assert np.isfinite(zero[emitted]).all()  # never emits a token the target gives no mass
+
+
+@pytest.mark.parametrize("what", ["token", "nan", "posinf", "uniform", "allneginf"])
+def test_data_errors_set_status_and_stay_in_range(lib, what):
+    inp = W.make_inputs(6, 3, 4000, dtype=torch.float32, seed=11, name=what)
+    if what == "token":
+        inp.tokens[2, 1] = 4000
+    elif what == "nan":
+        inp.target[3, 2, 17] = float("nan")
+    elif what == "posinf":
+        inp.draft[1, 0, 5] = float("inf")
+    elif what == "uniform":
+        inp.uniforms[4, 3] = 1.0
+    else:
+        inp.target[0, 1, :] = float("-inf")
+    g, ref = run_gpu(lib, inp), run_oracle(inp)
+    assert int(g["status"][0]) == ref["status"] != 0
+    assert ((g["accepted_len"] >= 0) & (g["accepted_len"] <= 3)).all()
+    assert ((g["out_tokens"] >= -1) & (g["out_tokens"] < 4000)).all()
+    # sequences without a data error are unaffected
+    good = ref["accepted_len"] >= 0
+    ok = good & (ref["flags"] == 0)
+    np.testing.assert_array_equal(g["accepted_len"][ok], ref["accepted_len"][ok])
+    np.testing.assert_array_equal(g["out_tokens"][ok], ref["out_tokens"][ok])
+
+
+def test_greedy_data_errors(lib):
+    inp = W.make_inputs(5, 3, 3000, dtype=torch.bfloat16, mode=W.MODE_GREEDY, seed=12)
+    inp.target[1, 2, 100] = float("nan")
+    inp.tokens[3, 0] = -5
+    g, ref = run_gpu(lib, inp), run_oracle(inp)
+    assert int(g["status"][0]) == ref["status"] == 3
+
+
+def test_deterministic_and_workspace_left_zero(lib):
+    inp = W.make_inputs(64, 5, 50000, dtype=torch.bfloat16, temperature=0.9, target_std=4.0,
+                        draft_noise=1.0, seed=13)
+    dev = [_dev(t) for t in (inp.target, inp.draft, inp.tokens, inp.uniforms)]
+    nbytes = lib.workspace_size(64, 5, 50000, lib.DTYPE_BF16, lib.MODE_SAMPLE)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    first = None
+    for _ in range(20):
+        acc, out = lib.verify(*dev, inp.temperature, "sample", workspace=ws)
+        torch.cuda.synchronize()
+        cur = (acc.cpu().numpy(), out.cpu().numpy())
+        if first is None:
+            first = cur
+        assert np.array_equal(cur[0], first[0]) and np.array_equal(cur[1], first[1])
+    # the per-sequence state (counters, masks) is back to zero after each call
+    seq = ws[: 64 * 32].view(torch.int64)
+    assert int(seq.count_nonzero().item()) == 0
+    g = W.make_inputs(64, 8, 32000, dtype=torch.bfloat16, mode=W.MODE_GREEDY, seed=14)
+    wsg = torch.zeros(lib.workspace_size(64, 8, 32000, 1, 1), dtype=torch.uint8, device="cuda")
+    lib.verify(_dev(g.target), None, _dev(g.tokens), None, 1.0, "greedy", workspace=wsg)
+    torch.cuda.synchronize()
+    assert int(wsg.count_nonzero().item()) == 0
+
+
+def test_greedy_ignores_draft_uniforms_and_temperature(lib):
+    inp = W.make_inputs(4, 3, 1000, dtype=torch.float32, mode=W.MODE_GREEDY, seed=15)
+    acc, out = lib.verify(_dev(inp.target), None, _dev(inp.tokens), None, float("nan"), "greedy")
+    ref = run_oracle(inp)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref["out_tokens"])
+
+
+def test_host_tensors_roundtrip_through_the_device(lib):
+    inp = W.make_inputs(8, 4, 3000, dtype=torch.float32, seed=16)
+    acc, out = lib.verify(inp.target.pin_memory(), inp.draft.pin_memory(),
+                          inp.tokens.pin_memory(), inp.uniforms.pin_memory(), 1.0, "sample")
+    assert not acc.is_cuda
+    ref = run_oracle(inp)
+    ok = ref["flags"] == 0
+    np.testing.assert_array_equal(out.numpy()[ok], ref["out_tokens"][ok])
+
+
+def test_bad_arguments_raise_before_launch(lib):
+    t = torch.zeros((2, 3, 10), device="cuda")
+    with pytest.raises(ValueError):
+        lib.verify(t, torch.zeros((2, 2, 10), device="cuda"), torch.zeros((2, 2), dtype=torch.int64,
+                   device="cuda"), torch.zeros((2, 3), device="cuda"), 1.0)
+    with pytest.raises(lib.SpecVerifyError):
+        lib.verify(t, torch.zeros((2, 2, 10), device="cuda"),
+                   torch.zeros((2, 2), dtype=torch.int32, device="cuda"),
+                   torch.zeros((2, 3), device="cuda"), 0.0)
