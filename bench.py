@@ -224,12 +224,13 @@ def device_time(binding, inp, steps, warmup, dev, l2_bytes):
     if steps % G:
         plan.append([g for n, g in graphs if n == steps % G][0])
     # one untimed replay of each graph
-    for _, g in graphs:
-        g.replay()
+    with torch.cuda.stream(stream):
+        for _, g in graphs:
+            g.replay()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    return R, nbytes, stream, plan, e0, e1
+    return R, nbytes, stream, plan, e0, e1, (acc, out)
 
 
 def run_native(args, rank, world, local):
@@ -241,7 +242,9 @@ def run_native(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     inp = W.workload(args.workload, seed=shard_seed(0, rank))
-    R, nbytes, stream, plan, e0, e1 = device_time(binding, inp, args.steps, args.warmup, dev, l2)
+    R, nbytes, stream, plan, e0, e1, acc_out = device_time(binding, inp, args.steps, args.warmup,
+                                                           dev, l2)
+    acc_out[0].fill_(-1)
 
     clocks = ClockSampler(local)
     if rank == 0:
@@ -249,13 +252,18 @@ def run_native(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    e0.record(stream)
-    for g in plan:
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):  # graphs replay on the current stream
+        e0.record(stream)
+        for g in plan:
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
     barrier(world)
+    # the replayed graphs wrote real outputs (guards against timing an empty graph)
+    n_host = acc_out[0].cpu()
+    if not (int(n_host.min()) >= 0 and int(n_host.max()) <= inp.K):
+        raise RuntimeError("timed launches did not produce valid outputs")
     clk = clocks.stop(t0, t1) if rank == 0 else None
     sec = e0.elapsed_time(e1) / 1e3
     sec_max = max_over_ranks(sec, world)
@@ -328,12 +336,13 @@ def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
         if name == skip:
             continue
         inp = W.workload(name)
-        R, nbytes, stream, plan, e0, e1 = device_time(binding, inp, steps, 5, dev, l2)
+        R, nbytes, stream, plan, e0, e1, _ = device_time(binding, inp, steps, 5, dev, l2)
         torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for g in plan:
-            g.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g in plan:
+                g.replay()
+            e1.record(stream)
         torch.cuda.synchronize(dev)
         sec = e0.elapsed_time(e1) / 1e3 / steps
         table[name] = {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec,

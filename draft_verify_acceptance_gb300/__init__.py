@@ -20,6 +20,7 @@ MODE_GREEDY = 1
 
 def __getattr__(name):
     if name in ("verify", "verify_ex", "workspace_size", "binding"):
-        from . import binding
+        import importlib
+        binding = importlib.import_module(__name__ + ".binding")
         return binding if name == "binding" else getattr(binding, name)
     raise AttributeError(name)

@@ -114,6 +114,9 @@ __device__ void finalize_sequence(const VerifyArgs& a, int b) {
     const unsigned long long evaluated = (n >= 63) ? ~0ull : ((2ull << n) - 1ull);
     a.flags[b] = ((near & evaluated) ? kFlagRatio : 0u) | ((c < 0) ? kFlagCdf : 0u);
   }
+  // leave this sequence's part of the workspace zero-filled for the next call
+  volatile int32_t* wslots = static_cast<volatile int32_t*>(a.slots);
+  for (int j = 0; j < K1; ++j) wslots[2 * (static_cast<size_t>(b) * K1 + j)] = 0;
   st->reject_mask = 0ull;
   st->near_mask = 0ull;
   st->arrivals = 0u;

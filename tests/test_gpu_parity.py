@@ -231,9 +231,8 @@ def test_deterministic_and_workspace_left_zero(lib):
         if first is None:
             first = cur
         assert np.array_equal(cur[0], first[0]) and np.array_equal(cur[1], first[1])
-    # the per-sequence state (counters, masks) is back to zero after each call
-    seq = ws[: 64 * 32].view(torch.int64)
-    assert int(seq.count_nonzero().item()) == 0
+    # the whole workspace (counters, masks, candidates) is back to zero
+    assert int(ws.count_nonzero().item()) == 0
     g = W.make_inputs(64, 8, 32000, dtype=torch.bfloat16, mode=W.MODE_GREEDY, seed=14)
     wsg = torch.zeros(lib.workspace_size(64, 8, 32000, 1, 1), dtype=torch.uint8, device="cuda")
     lib.verify(_dev(g.target), None, _dev(g.tokens), None, 1.0, "greedy", workspace=wsg)
@@ -260,7 +259,7 @@ def test_host_tensors_roundtrip_through_the_device(lib):
 
 def test_bad_arguments_raise_before_launch(lib):
     t = torch.zeros((2, 3, 10), device="cuda")
-    with pytest.raises(ValueError):
+    with pytest.raises(TypeError):
         lib.verify(t, torch.zeros((2, 2, 10), device="cuda"), torch.zeros((2, 2), dtype=torch.int64,
                    device="cuda"), torch.zeros((2, 3), device="cuda"), 1.0)
     with pytest.raises(lib.SpecVerifyError):
