@@ -26,6 +26,8 @@ OK = 0
 ERR_INVALID_ARG = 1
 ERR_UNSUPPORTED = 2
 ERR_CUDA = 3
+ERR_SCRATCH_LIMIT = 4
+STATIC_SCRATCH_BYTES = 1 << 20
 
 DATA_TOKEN_RANGE = 1
 DATA_NONFINITE_LOGIT = 2
@@ -33,7 +35,8 @@ DATA_UNIFORM_RANGE = 4
 FLAG_RATIO = 1
 FLAG_CDF = 2
 
-EXPORTS = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_status_string")
+EXPORTS = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_status_string",
+           "spec_verify_static")
 
 
 class SpecVerifyError(RuntimeError):
@@ -55,6 +58,8 @@ def _load():
     lib.spec_verify.argtypes = [P, P, P, P, I, I, I, I, F, I, P, P, P, Z, P]
     lib.spec_verify_ex.restype = I
     lib.spec_verify_ex.argtypes = [P, P, P, P, I, I, I, I, F, I, P, P, P, Z, P, P, P, P, P]
+    lib.spec_verify_static.restype = I
+    lib.spec_verify_static.argtypes = [P, P, P, P, I, I, I, I, F, I, P, P, P]
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [I]
     return lib

@@ -140,6 +140,7 @@ const char* spec_status_string(int status) {
     case SPEC_ERR_INVALID_ARG: return "invalid argument";
     case SPEC_ERR_UNSUPPORTED: return "unsupported size";
     case SPEC_ERR_CUDA: return "CUDA error";
+    case SPEC_ERR_SCRATCH_LIMIT: return "batch needs more scratch than the static no-allocation buffer holds";
     default: return "unknown status";
   }
 }

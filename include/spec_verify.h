@@ -55,7 +55,9 @@ typedef enum {
   SPEC_OK = 0,
   SPEC_ERR_INVALID_ARG = 1,  /* bad pointer, size, dtype, mode, temperature or workspace */
   SPEC_ERR_UNSUPPORTED = 2,  /* valid request beyond this build's limits (K, V, grid) */
-  SPEC_ERR_CUDA = 3          /* a CUDA runtime call or launch failed */
+  SPEC_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  SPEC_ERR_SCRATCH_LIMIT = 4 /* spec_verify_static: the batch needs more scratch than
+                                SPEC_STATIC_SCRATCH_BYTES */
 } spec_status_t;
 
 typedef enum { SPEC_MODE_SAMPLE = 0, SPEC_MODE_GREEDY = 1 } spec_mode_t;
@@ -151,6 +153,44 @@ SPEC_API spec_status_t spec_verify_ex(const void* target_logits, const void* dra
                              size_t workspace_bytes, spec_stream_t stream,
                              float* p_at_draft, float* q_at_draft, uint32_t* flags,
                              int32_t* device_status);
+
+/*
+ * spec_verify_static -- spec_verify for callers that cannot allocate device
+ * memory.  (The pages have no counterpart: this is an interface convenience.)
+ *
+ * Some callers cannot hand spec_verify a workspace: a host program that only
+ * holds the logits and output buffers it was given by another runtime's
+ * memory pool (for example an inference server that reserves all device
+ * memory up front and forbids any other allocation), or a latency-critical
+ * decode loop in which cudaMalloc / cudaFree are not allowed because they can
+ * synchronise the device and take unbounded time.  This entry point takes the
+ * same inputs and outputs as spec_verify, minus the workspace, and allocates
+ * nothing: its scratch is a fixed array of SPEC_STATIC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits.
+ *
+ *   - The batch must fit: spec_verify_workspace_size(B, K, V, dtype, mode) must
+ *     not exceed SPEC_STATIC_SCRATCH_BYTES (for example B = 1024 with K = 64,
+ *     or B = 4096 with K = 16), else SPEC_ERR_SCRATCH_LIMIT and nothing is
+ *     queued.  Other argument errors are those of spec_verify.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with the device current) and does the
+ *     library's one-time kernel set-up; make that first call before any stream
+ *     capture is started.
+ *   - Every call shares the one array.  Each call clears the part it uses
+ *     (cudaMemsetAsync on `stream`) before its kernel, so it does not depend
+ *     on what the previous call left there; but calls that can overlap on the
+ *     GPU (different streams, or different host threads) race on it and must
+ *     not be issued concurrently.
+ *   - Asynchronous on `stream`, like spec_verify.  No cudaMalloc, cudaFree or
+ *     allocating library routine is called.
+ */
+#define SPEC_STATIC_SCRATCH_BYTES (1 << 20)
+SPEC_API spec_status_t spec_verify_static(const void* target_logits, const void* draft_logits,
+                                          const int32_t* draft_tokens, const float* uniforms,
+                                          int B, int K, int V, int dtype, float temperature,
+                                          int mode, int32_t* accepted_len, int32_t* out_tokens,
+                                          spec_stream_t stream);
 
 /* A short, static, human-readable description of a return code. */
 SPEC_API const char* spec_status_string(int status);

@@ -38,7 +38,8 @@ def _header_defines():
 def test_library_exports_every_declared_symbol(binding):
     names = _declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
-                          "spec_status_string"}
+                          "spec_status_string", "spec_verify_static"}
+    assert set(names) == set(binding.EXPORTS)
     lib = ctypes.CDLL(binding.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -56,6 +57,8 @@ def test_header_constants_match_binding(binding):
     assert d["SPEC_ERR_INVALID_ARG"] == binding.ERR_INVALID_ARG
     assert d["SPEC_ERR_UNSUPPORTED"] == binding.ERR_UNSUPPORTED
     assert d["SPEC_ERR_CUDA"] == binding.ERR_CUDA
+    assert d["SPEC_ERR_SCRATCH_LIMIT"] == binding.ERR_SCRATCH_LIMIT
+    assert d["SPEC_STATIC_SCRATCH_BYTES"] == binding.STATIC_SCRATCH_BYTES
     assert d["SPEC_MODE_SAMPLE"] == binding.MODE_SAMPLE
     assert d["SPEC_MODE_GREEDY"] == binding.MODE_GREEDY
     assert d["SPEC_DTYPE_F32"] == binding.DTYPE_F32
