@@ -32,6 +32,7 @@ STATIC_SCRATCH_BYTES = 1 << 20
 DATA_TOKEN_RANGE = 1
 DATA_NONFINITE_LOGIT = 2
 DATA_UNIFORM_RANGE = 4
+DEVICE_WAIT_TIMEOUT = 8
 FLAG_RATIO = 1
 FLAG_CDF = 2
 

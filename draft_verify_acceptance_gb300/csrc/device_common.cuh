@@ -12,10 +12,16 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;          // portable cluster size
 constexpr int kMaxTiles = 1024;         // tiles of kThreads vectors per CTA segment
 
-// Device status bits (same values as the public header's SPEC_DATA_*).
+// Device status bits (same values as the public header's SPEC_DATA_* and
+// SPEC_DEVICE_WAIT_TIMEOUT).
 constexpr int kDataTokenRange = 1;
 constexpr int kDataNonfiniteLogit = 2;
 constexpr int kDataUniformRange = 4;
+constexpr int kWaitTimeout = 8;
+// Bound on the polls of one mbarrier wait (each poll may suspend the thread
+// for a short hardware-defined time); past it the kernel reports
+// kWaitTimeout instead of waiting forever.
+constexpr unsigned int kMaxPolls = 1u << 22;
 // Per-sequence boundary flags (public SPEC_FLAG_*).
 constexpr uint32_t kFlagRatio = 1;
 constexpr uint32_t kFlagCdf = 2;
@@ -31,11 +37,17 @@ struct __align__(32) SeqState {
 };
 static_assert(sizeof(SeqState) == 32, "SeqState layout");
 
-// Workspace: SeqState[B] followed by one 8-byte slot per row (B*(K+1)):
-// the candidate token of a sampled row (int32 in the low word, bit 31 = CDF
-// near-boundary) or the packed argmax key of a greedy row.
+// One per row (B*(K+1) of them) after SeqState[B].  Zero at rest.
+struct __align__(16) RowSlot {
+  unsigned long long value;  // sampling: candidate token (low 31 bits) | CDF-near bit 31
+                             // greedy:   packed (orderable max, ~index) argmax key
+  unsigned int spare;        // unused (zero)
+  unsigned int pad;
+};
+static_assert(sizeof(RowSlot) == 16, "RowSlot layout");
+
 inline size_t workspace_bytes(long long B, long long K) {
-  size_t n = (size_t)B * sizeof(SeqState) + (size_t)B * (size_t)(K + 1) * 8;
+  size_t n = (size_t)B * sizeof(SeqState) + (size_t)B * (size_t)(K + 1) * sizeof(RowSlot);
   return (n + 255) & ~(size_t)255;
 }
 
@@ -110,6 +122,83 @@ template <>
 __device__ __forceinline__ float load_one<BF16>(const void* row, long long j) {
   uint16_t h = __ldg(static_cast<const unsigned short*>(row) + j);
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// ---- TMA bulk copies and mbarriers ---------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Arrive once on `bar` and announce `bytes` of transactions for this phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of
+// 16), completing `bytes` transactions on `bar`.  No multicast.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// One poll that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (the hardware wakes it when the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(unsigned long long* bar, uint32_t parity,
+                                                    uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` from ONE thread, sleeping between polls
+// instead of spinning (other threads of the CTA wait at a barrier and take
+// no issue slots).  At most 2^16 polls of <= 20 us each (~1.3 s), then false.
+__device__ __forceinline__ bool mbar_wait_one(unsigned long long* bar, uint32_t parity) {
+  for (unsigned int i = 0; i < (1u << 16); ++i)
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+  return false;
+}
+
+// Wait for phase `parity` of `bar` to complete, polling at most kMaxPolls
+// times.  Returns false on timeout (the caller reports kWaitTimeout).
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
+  for (unsigned int i = 0; i < kMaxPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 
 // ---- arithmetic ----------------------------------------------------------

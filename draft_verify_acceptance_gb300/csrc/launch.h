@@ -33,7 +33,7 @@ struct VerifyArgs {
 // Per-device facts gathered once.
 struct DeviceInfo {
   int sm_count = 0;
-  int greedy_ctas_per_sm = 0;  // occupancy of the greedy kernel (vector path)
+  int greedy_ctas_per_sm = 0;  // occupancy of the greedy kernel
 };
 
 cudaError_t device_info(int device, DeviceInfo* out);
@@ -45,5 +45,11 @@ long long sample_tiles(long long nvec, int cluster);
 
 cudaError_t launch_greedy(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// The sampling kernel that stages row slices in shared memory (16-byte
+// aligned rows whose slices fit); launch_sample dispatches to it.
+int sample_smem_cluster(long long nvec);
+cudaError_t sample_smem_prepare();
+cudaError_t launch_sample_smem(const VerifyArgs& a, int C, cudaStream_t stream);
 
 }  // namespace specv

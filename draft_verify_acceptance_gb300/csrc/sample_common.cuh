@@ -1,0 +1,129 @@
+// sample_common.cuh -- pieces shared by the two sampling kernels: the
+// fixed-point residual weights of one vector, and the warp-parallel
+// finalisation of a sequence.
+#pragma once
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace specv {
+
+constexpr float kFix = 72057594037927936.0f;  // 2^56: fixed-point scale of probabilities
+constexpr float kBandF = 1e-6f;               // boundary band of the ratio test
+
+// The residual weights r_k = max(0, p_k - q_k) (or p_k when `residual` is
+// false) of one vector and the vector's fixed-point mass round(2^56 * sum r).
+// The fp32 sum runs in element order with explicitly rounded operations, so
+// every recomputation is bit-identical and integer sums of masses agree
+// exactly in any order.
+template <int VEC>
+__device__ __forceinline__ unsigned long long vec_weight(const float (&xt)[VEC],
+                                                         const float (&xd)[VEC], float Mt,
+                                                         float invZt, float Md, float invZd,
+                                                         float s, bool residual,
+                                                         float (&r)[VEC]) {
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    const float pt = __fmul_rn(ex2(__fmul_rn(__fsub_rn(xt[k], Mt), s)), invZt);
+    float rk = pt;
+    if (residual) {
+      const float qd = __fmul_rn(ex2(__fmul_rn(__fsub_rn(xd[k], Md), s)), invZd);
+      rk = fmaxf(0.f, __fsub_rn(pt, qd));
+    }
+    r[k] = rk;
+    acc = __fadd_rn(acc, rk);
+  }
+  return __float2ull_rn(__fmul_rn(acc, kFix));
+}
+
+// The same weights with the normalisers kept relative to scaled offsets
+// MSt = round(Mt * s), MSd = round(Md * s): p_k = 2^fma(x_k, s, -MSt) / Zt.
+// One fused multiply-add per logit; the offset's rounding is common to every
+// term of the row and to its normaliser, so it cancels.
+template <int VEC>
+__device__ __forceinline__ unsigned long long vec_weight_scaled(
+    const float (&xt)[VEC], const float (&xd)[VEC], float MSt, float invZt, float MSd,
+    float invZd, float s, bool residual, float (&r)[VEC]) {
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    const float pt = __fmul_rn(ex2(__fmaf_rn(xt[k], s, -MSt)), invZt);
+    float rk = pt;
+    if (residual) {
+      const float qd = __fmul_rn(ex2(__fmaf_rn(xd[k], s, -MSd)), invZd);
+      rk = fmaxf(0.f, __fsub_rn(pt, qd));
+    }
+    r[k] = rk;
+    acc = __fadd_rn(acc, rk);
+  }
+  return __float2ull_rn(__fmul_rn(acc, kFix));
+}
+
+// Merge two normalisers kept relative to scaled offsets (ms, z): the result
+// is relative to the larger offset.  Subtracting two close offsets is exact.
+__device__ __forceinline__ void merge_scaled(float& ms, float& z, float ms2, float z2) {
+  const float mn = fmaxf(ms, ms2);
+  if (mn == -INFINITY) {
+    ms = mn;
+    z = 0.f;
+    return;
+  }
+  const float a = (ms == -INFINITY) ? 0.f : z * ex2(ms - mn);
+  const float b = (ms2 == -INFINITY) ? 0.f : z2 * ex2(ms2 - mn);
+  ms = mn;
+  z = a + b;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Candidate slot of row (b, i): the token in the low 31 bits, bit 31 set
+// when the draw was within the boundary band of a CDF step.
+__device__ __forceinline__ volatile int32_t* candidate_slot(const VerifyArgs& a, int b, int i) {
+  return reinterpret_cast<volatile int32_t*>(static_cast<RowSlot*>(a.slots) +
+                                             static_cast<size_t>(b) * (a.K + 1) + i);
+}
+
+// Counts one finished row of sequence b and, for the last of its K+1 rows,
+// finalises the sequence with the whole calling warp: n is the lowest
+// rejected position (K if none), the outputs are x_0..x_{n-1}, the candidate
+// of row n, then -1, and the sequence's workspace goes back to zero.  All 32
+// lanes of one warp must call this; lane 0 has already written the row's
+// candidate (if any) before the call.
+__device__ __forceinline__ void warp_arrive_and_finalize(const VerifyArgs& a, int b) {
+  const int lane = threadIdx.x & 31;
+  const int K = a.K, K1 = K + 1;
+  int last = 0;
+  if (lane == 0) last = arrive_last(a.seq, b, static_cast<unsigned int>(K1)) ? 1 : 0;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();  // every lane reads what the other rows published
+  __syncwarp();
+  SeqState* st = a.seq + b;
+  const unsigned long long mask = *reinterpret_cast<volatile unsigned long long*>(&st->reject_mask);
+  const unsigned long long near = *reinterpret_cast<volatile unsigned long long*>(&st->near_mask);
+  const int n = mask ? (__ffsll(static_cast<long long>(mask)) - 1) : K;
+  const int32_t c = *candidate_slot(a, b, n);
+  const int32_t* x = a.tokens + static_cast<size_t>(b) * K;
+  int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
+  for (int j = lane; j < K1; j += 32)
+    out[j] = (j < n) ? min(max(x[j], 0), a.V - 1) : (j == n ? (c & 0x7fffffff) : -1);
+  __syncwarp();
+  for (int j = lane; j < K1; j += 32) *candidate_slot(a, b, j) = 0;
+  if (lane == 0) {
+    a.accepted_len[b] = n;
+    if (a.flags) {
+      const unsigned long long evaluated = (n >= 63) ? ~0ull : ((2ull << n) - 1ull);
+      a.flags[b] = ((near & evaluated) ? kFlagRatio : 0u) | ((c < 0) ? kFlagCdf : 0u);
+    }
+    st->reject_mask = 0ull;
+    st->near_mask = 0ull;
+    st->arrivals = 0u;
+  }
+}
+
+}  // namespace specv

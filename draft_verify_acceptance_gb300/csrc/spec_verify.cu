@@ -29,6 +29,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = greedy_occupancy(&d.greedy_ctas_per_sm);
     if (e == cudaSuccess) e = sample_prepare();
+    if (e == cudaSuccess) e = sample_smem_prepare();
     g_info[device] = d;
     g_err[device] = e;
   });

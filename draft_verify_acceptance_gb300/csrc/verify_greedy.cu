@@ -108,16 +108,16 @@ greedy_kernel(VerifyArgs a, long long nvec, int S) {
   for (int w = 1; w < kWarps; ++w) argmax_merge(best, bidx, s_v[w], s_i[w]);
   if (any_bad && a.status) atomicOr(a.status, kDataNonfiniteLogit);
 
-  unsigned long long* keys = static_cast<unsigned long long*>(a.slots);
+  RowSlot* slots = static_cast<RowSlot*>(a.slots);
   const unsigned long long key = pack_key(best, bidx);
-  if (S == 1) keys[row] = key;
-  else atomicMax(&keys[row], key);
+  if (S == 1) slots[row].value = key;
+  else atomicMax(&slots[row].value, key);
 
   if (!arrive_last(a.seq, b, static_cast<unsigned int>(K1) * static_cast<unsigned int>(S)))
     return;
 
   // last arrival for sequence b: longest matching prefix, outputs, reset
-  volatile unsigned long long* vkeys = keys + static_cast<size_t>(b) * K1;
+  volatile RowSlot* vslots = slots + static_cast<size_t>(b) * K1;
   const int32_t* x = a.tokens + static_cast<size_t>(b) * a.K;
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
   int n = a.K;
@@ -125,15 +125,15 @@ greedy_kernel(VerifyArgs a, long long nvec, int S) {
   for (int i = 0; i < a.K; ++i) {
     const int xi = x[i];
     bad_tok |= (xi < 0 || xi >= a.V);
-    if (n == a.K && xi != key_index(vkeys[i])) n = i;
+    if (n == a.K && xi != key_index(vslots[i].value)) n = i;
   }
   for (int i = 0; i < n; ++i) out[i] = x[i];
-  out[n] = key_index(vkeys[n]);
+  out[n] = key_index(vslots[n].value);
   for (int i = n + 1; i < K1; ++i) out[i] = -1;
   a.accepted_len[b] = n;
   if (a.flags) a.flags[b] = 0;
   if (bad_tok && a.status) atomicOr(a.status, kDataTokenRange);
-  for (int i = 0; i < K1; ++i) vkeys[i] = 0ull;
+  for (int i = 0; i < K1; ++i) vslots[i].value = 0ull;
   a.seq[b].arrivals = 0u;
 }
 

@@ -39,15 +39,13 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "sample_common.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace specv {
 
 namespace {
-
-constexpr float kFix = 72057594037927936.0f;  // 2^56: fixed-point scale of probabilities
-constexpr float kBandF = 1e-6f;
 
 // Online update of (m, z) with a register chunk.
 template <int N>
@@ -65,36 +63,6 @@ __device__ __forceinline__ void online_chunk(float& m, float& z, const float* x,
   }
 }
 
-// The residual (or target) weights of one vector and their fixed-point sum.
-// Every operation is an explicitly rounded intrinsic, so pass 2 and pass 3
-// produce bit-identical values.
-template <int VEC>
-__device__ __forceinline__ unsigned long long vec_weight(const float (&xt)[VEC],
-                                                         const float (&xd)[VEC], float Mt,
-                                                         float invZt, float Md, float invZd,
-                                                         float s, bool residual,
-                                                         float (&r)[VEC]) {
-  float acc = 0.f;
-#pragma unroll
-  for (int k = 0; k < VEC; ++k) {
-    const float pt = __fmul_rn(ex2(__fmul_rn(__fsub_rn(xt[k], Mt), s)), invZt);
-    float rk = pt;
-    if (residual) {
-      const float qd = __fmul_rn(ex2(__fmul_rn(__fsub_rn(xd[k], Md), s)), invZd);
-      rk = fmaxf(0.f, __fsub_rn(pt, qd));
-    }
-    r[k] = rk;
-    acc = __fadd_rn(acc, rk);
-  }
-  return __float2ull_rn(__fmul_rn(acc, kFix));
-}
-
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
 // Finalise sequence b (called by the single last arrival).
 __device__ void finalize_sequence(const VerifyArgs& a, int b) {
   const int K = a.K, K1 = K + 1;
@@ -103,7 +71,7 @@ __device__ void finalize_sequence(const VerifyArgs& a, int b) {
   const unsigned long long near = *reinterpret_cast<volatile unsigned long long*>(&st->near_mask);
   const int n = mask ? (__ffsll(static_cast<long long>(mask)) - 1) : K;
   const volatile int32_t* slots = static_cast<const volatile int32_t*>(a.slots);
-  const int32_t c = slots[2 * (static_cast<size_t>(b) * K1 + n)];
+  const int32_t c = slots[4 * (static_cast<size_t>(b) * K1 + n)];
   const int32_t* x = a.tokens + static_cast<size_t>(b) * K;
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
   for (int j = 0; j < n; ++j) out[j] = min(max(x[j], 0), a.V - 1);
@@ -116,7 +84,7 @@ __device__ void finalize_sequence(const VerifyArgs& a, int b) {
   }
   // leave this sequence's part of the workspace zero-filled for the next call
   volatile int32_t* wslots = static_cast<volatile int32_t*>(a.slots);
-  for (int j = 0; j < K1; ++j) wslots[2 * (static_cast<size_t>(b) * K1 + j)] = 0;
+  for (int j = 0; j < K1; ++j) wslots[4 * (static_cast<size_t>(b) * K1 + j)] = 0;
   st->reject_mask = 0ull;
   st->near_mask = 0ull;
   st->arrivals = 0u;
@@ -156,7 +124,7 @@ sample_kernel(VerifyArgs a, long long nvec, int ntiles) {
   const float s = a.scale;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int32_t* slots = static_cast<int32_t*>(a.slots);
-  const size_t my_slot = 2 * (static_cast<size_t>(b) * K1 + i);
+  const size_t my_slot = 4 * (static_cast<size_t>(b) * K1 + i);
 
   __shared__ float s_part[kMaxCluster][4];               // pushed by each rank
   __shared__ float s_red[kWarps][4];
@@ -435,6 +403,11 @@ cudaError_t sample_prepare() {
 }
 
 cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo&, cudaStream_t stream) {
+  if (a.vec) {
+    const int C = sample_smem_cluster(static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16);
+    if (C > 0) return launch_sample_smem(a, C, stream);
+  }
+  // unaligned rows, or rows too long to stage: the streaming kernel below
   if (a.bf16) {
     return a.vec ? launch_sample_t<BF16, 8, 4>(a, stream)
                  : launch_sample_t<BF16, 1, 8>(a, stream);

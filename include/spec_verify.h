@@ -72,6 +72,9 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 #define SPEC_DATA_TOKEN_RANGE 1      /* a draft token outside [0, V) (clamped) */
 #define SPEC_DATA_NONFINITE_LOGIT 2  /* NaN or +inf logit, or a row with no finite entry */
 #define SPEC_DATA_UNIFORM_RANGE 4    /* a uniform outside [0, 1) or NaN */
+/* Not a data error: a kernel's bounded wait for its own bulk copies gave up
+ * (outputs of that call are unspecified).  Never expected in normal use. */
+#define SPEC_DEVICE_WAIT_TIMEOUT 8
 
 /* Per-sequence boundary flags (sampling mode; written when `flags` is given).
  * They mark decisions the kernel took within 1e-6 of a threshold, where a

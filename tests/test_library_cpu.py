@@ -68,6 +68,7 @@ def test_header_constants_match_binding(binding):
     assert d["SPEC_DATA_TOKEN_RANGE"] == binding.DATA_TOKEN_RANGE
     assert d["SPEC_DATA_NONFINITE_LOGIT"] == binding.DATA_NONFINITE_LOGIT
     assert d["SPEC_DATA_UNIFORM_RANGE"] == binding.DATA_UNIFORM_RANGE
+    assert d["SPEC_DEVICE_WAIT_TIMEOUT"] == binding.DEVICE_WAIT_TIMEOUT
     assert d["SPEC_FLAG_RATIO"] == binding.FLAG_RATIO
     assert d["SPEC_FLAG_CDF"] == binding.FLAG_CDF
 
