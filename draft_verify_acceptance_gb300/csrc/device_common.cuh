@@ -46,10 +46,32 @@ struct __align__(16) RowSlot {
 };
 static_assert(sizeof(RowSlot) == 16, "RowSlot layout");
 
-inline size_t workspace_bytes(long long B, long long K) {
-  size_t n = (size_t)B * sizeof(SeqState) + (size_t)B * (size_t)(K + 1) * sizeof(RowSlot);
-  return (n + 255) & ~(size_t)255;
+// Partial softmax normalisers of one (CTA, row pair) of the streaming pass,
+// relative to scaled offsets: target (ms_t, z_t), draft (ms_d, z_d).
+struct __align__(16) Partial {
+  float ms_t, z_t, ms_d, z_d;
+};
+
+// Largest persistent grid of the streaming pass.  Its partials need at most
+// kMaxStreamCtas + rows slots (contributor c of row pair p writes slot c + p).
+constexpr long long kMaxStreamCtas = 4096;
+
+// Workspace layout: SeqState[B] | RowSlot[R] | Partial[kMaxStreamCtas + R + 1]
+// | float2 gathers[R]   (R = B*(K+1) rows; every part 16-byte aligned).
+struct WorkspaceLayout {
+  size_t seq, slots, partials, gathers, total;
+};
+inline WorkspaceLayout workspace_layout(long long B, long long K) {
+  const size_t R = (size_t)B * (size_t)(K + 1);
+  WorkspaceLayout l;
+  l.seq = 0;
+  l.slots = l.seq + (size_t)B * sizeof(SeqState);
+  l.partials = l.slots + R * sizeof(RowSlot);
+  l.gathers = l.partials + ((size_t)kMaxStreamCtas + R + 1) * sizeof(Partial);
+  l.total = ((l.gathers + R * 8) + 255) & ~(size_t)255;
+  return l;
 }
+inline size_t workspace_bytes(long long B, long long K) { return workspace_layout(B, K).total; }
 
 #ifdef __CUDACC__
 
@@ -193,12 +215,36 @@ __device__ __forceinline__ bool mbar_wait_one(unsigned long long* bar, uint32_t 
   return false;
 }
 
+// Wait for phase `parity` of `bar` from any number of threads; each blocks
+// in hardware between polls (no spinning).  At most 2^16 polls of <= 20 us.
+__device__ __forceinline__ bool mbar_wait_sleep(unsigned long long* bar, uint32_t parity) {
+  for (unsigned int i = 0; i < (1u << 16); ++i)
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+  return false;
+}
+
+// Plain arrival (count 1) on `bar`.
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Wait for phase `parity` of `bar` to complete, polling at most kMaxPolls
 // times.  Returns false on timeout (the caller reports kWaitTimeout).
 __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
   for (unsigned int i = 0; i < kMaxPolls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+
+// ---- cluster barrier, split -----------------------------------------------
+// Every thread of every CTA of the cluster arrives early and waits just
+// before its first access to another CTA's shared memory: that access must
+// not come before all CTAs of the cluster have started.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // ---- arithmetic ----------------------------------------------------------

@@ -75,10 +75,73 @@ __device__ __forceinline__ void merge_scaled(float& ms, float& z, float ms2, flo
   z = a + b;
 }
 
+// Warp-wide merge of (ms, z) normalisers: the warp's largest offset, one
+// rescale per lane, then a butterfly sum (every lane ends with the same bits:
+// each step adds the same two values on both partners).
+__device__ __forceinline__ void warp_merge_scaled(float& ms, float& z) {
+  float M = ms;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float zz = (ms == -INFINITY) ? 0.f : z * ex2(ms - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+  ms = M;
+  z = (M == -INFINITY) ? 0.f : zz;
+}
+
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
+}
+
+// 16-byte staged vectors: unpacking and a NaN-ignoring running maximum.
+template <typename E>
+struct Staged;
+
+template <>
+struct Staged<BF16> {
+  static constexpr int kVec = 8;
+  using Max = uint32_t;  // packed bf16x2 running maximum
+  static __device__ __forceinline__ Max max_init() { return 0xff80ff80u; }  // (-inf, -inf)
+  static __device__ __forceinline__ uint32_t bmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ void max_update(Max& m, const uint4 w) {
+    m = bmax(m, bmax(bmax(w.x, w.y), bmax(w.z, w.w)));
+  }
+  static __device__ __forceinline__ float max_value(Max m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
+  static __device__ __forceinline__ void unpack(const uint4 w, float (&x)[8]) {
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+  }
+};
+
+template <>
+struct Staged<F32> {
+  static constexpr int kVec = 4;
+  using Max = float;
+  static __device__ __forceinline__ Max max_init() { return -INFINITY; }
+  static __device__ __forceinline__ void max_update(Max& m, const uint4 w) {
+    m = fmaxf(fmaxf(m, fmaxf(__uint_as_float(w.x), __uint_as_float(w.y))),
+              fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+  }
+  static __device__ __forceinline__ float max_value(Max m) { return m; }
+  static __device__ __forceinline__ void unpack(const uint4 w, float (&x)[4]) {
+    x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+  }
+};
+
+// One element of a staged slice.
+template <typename E>
+__device__ __forceinline__ float staged_elem(const uint4* slice, int j) {
+  if constexpr (Staged<E>::kVec == 8)
+    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(slice)[j]) << 16);
+  else
+    return reinterpret_cast<const float*>(slice)[j];
 }
 
 // Candidate slot of row (b, i): the token in the low 31 bits, bit 31 set

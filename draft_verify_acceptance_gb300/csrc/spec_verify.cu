@@ -30,6 +30,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     if (e == cudaSuccess) e = greedy_occupancy(&d.greedy_ctas_per_sm);
     if (e == cudaSuccess) e = sample_prepare();
     if (e == cudaSuccess) e = sample_smem_prepare();
+    if (e == cudaSuccess) e = sample_2p_prepare(&d.stream_ctas_per_sm);
     g_info[device] = d;
     g_err[device] = e;
   });
@@ -110,8 +111,11 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   a.q_at = sample ? q_at_draft : nullptr;
   a.flags = flags;
   a.status = device_status;
-  a.seq = static_cast<specv::SeqState*>(workspace);
-  a.slots = static_cast<char*>(workspace) + static_cast<size_t>(B) * sizeof(specv::SeqState);
+  const specv::WorkspaceLayout lay = specv::workspace_layout(B, K);
+  a.seq = reinterpret_cast<specv::SeqState*>(static_cast<char*>(workspace) + lay.seq);
+  a.slots = static_cast<char*>(workspace) + lay.slots;
+  a.partials = static_cast<char*>(workspace) + lay.partials;
+  a.gathers = static_cast<char*>(workspace) + lay.gathers;
 
   const long long rows = static_cast<long long>(B) * (K + 1);
   if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;

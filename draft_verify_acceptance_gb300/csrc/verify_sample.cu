@@ -132,6 +132,7 @@ sample_kernel(VerifyArgs a, long long nvec, int ntiles) {
   __shared__ unsigned long long s_mass[2][kMaxCluster];   // pushed by each rank
   extern __shared__ unsigned long long s_tws[];           // [ntiles][kWarps]
 
+  cluster_arrive_relaxed();  // matched by cluster_wait() before the first DSMEM push
   // ---- pass 1: online normalisers of target row i and draft row i -------
   float mt = -INFINITY, zt = 0.f, md = -INFINITY, zd = 0.f;
   for (long long v = v0 + tid; v < v1; v += static_cast<long long>(kThreads) * U) {
@@ -155,6 +156,7 @@ sample_kernel(VerifyArgs a, long long nvec, int ntiles) {
     s_red[warp][0] = mt; s_red[warp][1] = zt; s_red[warp][2] = md; s_red[warp][3] = zd;
   }
   __syncthreads();
+  cluster_wait();  // every CTA of the cluster has started
   if (tid < C) {
     float m0 = s_red[0][0], z0 = s_red[0][1], m1 = s_red[0][2], z1 = s_red[0][3];
     for (int w = 1; w < kWarps; ++w) {
@@ -402,9 +404,12 @@ cudaError_t sample_prepare() {
   return prepare_t<F32, 1, 8>();
 }
 
-cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo&, cudaStream_t stream) {
+cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   if (a.vec) {
-    const int C = sample_smem_cluster(static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16);
+    const long long nvec = static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16;
+    const int C2 = sample_2p_cluster(nvec);
+    if (C2 > 0) return launch_sample_2p(a, dev, C2, stream);
+    const int C = sample_smem_cluster(nvec);
     if (C > 0) return launch_sample_smem(a, C, stream);
   }
   // unaligned rows, or rows too long to stage: the streaming kernel below

@@ -51,55 +51,6 @@ constexpr int kMaxC = 8;                  // largest cluster (portable size)
 constexpr int kProducer = kThreads - 32;  // issues the bulk copies
 constexpr int kSmemTarget = 72 * 1024;    // slice bytes for three CTAs per SM
 
-// 16-byte staged vectors: unpacking and a NaN-ignoring running maximum.
-template <typename E>
-struct Staged;
-
-template <>
-struct Staged<BF16> {
-  static constexpr int kVec = 8;
-  using Max = uint32_t;  // packed bf16x2 running maximum
-  static __device__ __forceinline__ Max max_init() { return 0xff80ff80u; }  // (-inf, -inf)
-  static __device__ __forceinline__ uint32_t bmax(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
-  static __device__ __forceinline__ void max_update(Max& m, const uint4 w) {
-    m = bmax(m, bmax(bmax(w.x, w.y), bmax(w.z, w.w)));
-  }
-  static __device__ __forceinline__ float max_value(Max m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
-  static __device__ __forceinline__ void unpack(const uint4 w, float (&x)[8]) {
-    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
-  }
-};
-
-template <>
-struct Staged<F32> {
-  static constexpr int kVec = 4;
-  using Max = float;
-  static __device__ __forceinline__ Max max_init() { return -INFINITY; }
-  static __device__ __forceinline__ void max_update(Max& m, const uint4 w) {
-    m = fmaxf(fmaxf(m, fmaxf(__uint_as_float(w.x), __uint_as_float(w.y))),
-              fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
-  }
-  static __device__ __forceinline__ float max_value(Max m) { return m; }
-  static __device__ __forceinline__ void unpack(const uint4 w, float (&x)[4]) {
-    x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
-    x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
-  }
-};
-
-// One element of a staged slice.
-template <typename E>
-__device__ __forceinline__ float staged_elem(const uint4* slice, int j) {
-  if constexpr (Staged<E>::kVec == 8)
-    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(slice)[j]) << 16);
-  else
-    return reinterpret_cast<const float*>(slice)[j];
-}
-
 // Per-thread normaliser of a slice relative to the scaled offset
 // ms = round(max(x) * s): z = sum 2^fma(x, s, -ms).
 template <typename E>
@@ -162,6 +113,7 @@ sample_smem_kernel(VerifyArgs a, long long nvec, int nvs) {
   __shared__ unsigned long long s_mass[2][kMaxC];      // pushed by each rank
   __shared__ float s_uK;
 
+  cluster_arrive_relaxed();  // matched by cluster_wait() before the first DSMEM push
   if (tid == 0) {
     mbar_init(&bar, 1);
     fence_barrier_init();
@@ -207,6 +159,7 @@ sample_smem_kernel(VerifyArgs a, long long nvec, int nvs) {
     s_red[warp][0] = mt; s_red[warp][1] = zt; s_red[warp][2] = md; s_red[warp][3] = zd;
   }
   __syncthreads();
+  cluster_wait();  // every CTA of the cluster has started
   if (tid < C) {
     float m0 = s_red[0][0], z0 = s_red[0][1], m1 = s_red[0][2], z1 = s_red[0][3];
     for (int w = 1; w < kWarps; ++w) {

@@ -173,8 +173,8 @@ SPEC_API spec_status_t spec_verify_ex(const void* target_logits, const void* dra
  * exits.
  *
  *   - The batch must fit: spec_verify_workspace_size(B, K, V, dtype, mode) must
- *     not exceed SPEC_STATIC_SCRATCH_BYTES (for example B = 1024 with K = 64,
- *     or B = 4096 with K = 16), else SPEC_ERR_SCRATCH_LIMIT and nothing is
+ *     not exceed SPEC_STATIC_SCRATCH_BYTES (for example B = 1024 with K = 16,
+ *     or B = 4096 with K = 4), else SPEC_ERR_SCRATCH_LIMIT and nothing is
  *     queued.  Other argument errors are those of spec_verify.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress, with the device current) and does the
