@@ -46,32 +46,55 @@ struct __align__(16) RowSlot {
 };
 static_assert(sizeof(RowSlot) == 16, "RowSlot layout");
 
-// Partial softmax normalisers of one (CTA, row pair) of the streaming pass,
-// relative to scaled offsets: target (ms_t, z_t), draft (ms_d, z_d).
+// Partial softmax normalisers of one work unit (a segment of a target row
+// and of the matching draft row) of the sampling kernel, relative to scaled
+// offsets: target (ms_t, z_t), draft (ms_d, z_d).
 struct __align__(16) Partial {
   float ms_t, z_t, ms_d, z_d;
 };
 
-// Largest persistent grid of the streaming pass.  Its partials need at most
-// kMaxStreamCtas + rows slots (contributor c of row pair p writes slot c + p).
-constexpr long long kMaxStreamCtas = 4096;
+// Work units of the fused sampling kernel: each draft position's (target,
+// draft) row pair is cut into segments of kFusedSeg 16-byte vectors, the bonus
+// target row into segments of twice that; a sequence has
+// fused_tasks_per_seq(K, nvec) of them and the workspace one Partial each.
+constexpr int kFusedSeg = 4096;
+inline long long fused_tasks_per_seq(long long K, long long nvec) {
+  const long long segs = (nvec + kFusedSeg - 1) / kFusedSeg;
+  const long long segs_b = (nvec + 2 * kFusedSeg - 1) / (2 * kFusedSeg);
+  return K * segs + segs_b;
+}
 
-// Workspace layout: SeqState[B] | RowSlot[R] | Partial[kMaxStreamCtas + R + 1]
-// | float2 gathers[R]   (R = B*(K+1) rows; every part 16-byte aligned).
-struct WorkspaceLayout {
-  size_t seq, slots, partials, gathers, total;
+// Claim counters of the fused sampling kernel.  Zero at rest: the last CTA
+// to finish puts them back.
+struct __align__(16) FusedCtl {
+  unsigned long long next_task;  // next work unit to hand out
+  unsigned long long done_ctas;  // CTAs that have taken their last unit
 };
-inline WorkspaceLayout workspace_layout(long long B, long long K) {
+
+// Workspace layout: SeqState[B] | units | FusedCtl, 16-byte aligned parts,
+// where `units` is either RowSlot[B*(K+1)] (greedy kernel, streaming sampler)
+// or Partial[B * tasks_per_seq] (fused sampler).  One call uses one of the
+// two views and leaves the region zero-filled, so both views can share it.
+// The size is taken for 16-byte vectors of the row (ceil(V*bytes/16)).
+struct WorkspaceLayout {
+  size_t seq, units, ctl, total;
+};
+inline WorkspaceLayout workspace_layout(long long B, long long K, long long V, int elem_bytes) {
   const size_t R = (size_t)B * (size_t)(K + 1);
+  const long long nvec = (V * elem_bytes + 15) / 16;
+  const size_t P = (size_t)B * (size_t)fused_tasks_per_seq(K, nvec);
   WorkspaceLayout l;
   l.seq = 0;
-  l.slots = l.seq + (size_t)B * sizeof(SeqState);
-  l.partials = l.slots + R * sizeof(RowSlot);
-  l.gathers = l.partials + ((size_t)kMaxStreamCtas + R + 1) * sizeof(Partial);
-  l.total = ((l.gathers + R * 8) + 255) & ~(size_t)255;
+  l.units = l.seq + (size_t)B * sizeof(SeqState);
+  const size_t ub = (R * sizeof(RowSlot) > P * sizeof(Partial)) ? R * sizeof(RowSlot)
+                                                                : P * sizeof(Partial);
+  l.ctl = l.units + ub;
+  l.total = ((l.ctl + sizeof(FusedCtl)) + 255) & ~(size_t)255;
   return l;
 }
-inline size_t workspace_bytes(long long B, long long K) { return workspace_layout(B, K).total; }
+inline size_t workspace_bytes(long long B, long long K, long long V, int elem_bytes) {
+  return workspace_layout(B, K, V, elem_bytes).total;
+}
 
 #ifdef __CUDACC__
 
@@ -191,6 +214,19 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
   return ok != 0;
 }
 
+// Non-blocking test: has phase `parity` of `bar` completed?
+__device__ __forceinline__ bool mbar_test(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // One poll that may suspend the thread for up to `ns` nanoseconds while the
 // phase is incomplete (the hardware wakes it when the phase completes).
 __device__ __forceinline__ bool mbar_try_wait_sleep(unsigned long long* bar, uint32_t parity,
@@ -267,6 +303,18 @@ __device__ __forceinline__ void merge_mz(float& m, float& z, float m2, float z2,
   float b = (m2 == -INFINITY) ? 0.f : z2 * ex2((m2 - mn) * s);
   m = mn;
   z = a + b;
+}
+
+// Add to a counter in global memory with acquire-release semantics at GPU
+// scope: this thread's earlier writes are visible to whoever observes the
+// new value, and what the earlier adders wrote is visible to this thread.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 // ---- workspace arrival ---------------------------------------------------

@@ -27,16 +27,16 @@ struct VerifyArgs {
   uint32_t* flags;             // [B] or null
   int32_t* status;             // device status word or null
   SeqState* seq;               // workspace: [B]
-  void* slots;                 // workspace: [B*(K+1)] RowSlot
-  void* partials;              // workspace: Partial slots of the streaming pass
-  void* gathers;               // workspace: [B*(K+1)] float2 (t[x_i], d[x_i])
+  void* slots;                 // workspace: [B*(K+1)] RowSlot (greedy, streaming sampler)
+  void* partials;              // workspace: Partial per work unit (fused sampler); same
+                               // region as `slots`
+  void* ctl;                   // workspace: FusedCtl
 };
 
 // Per-device facts gathered once.
 struct DeviceInfo {
   int sm_count = 0;
   int greedy_ctas_per_sm = 0;  // occupancy of the greedy kernel
-  int stream_ctas_per_sm = 0;  // occupancy of the normaliser stream kernel
 };
 
 cudaError_t device_info(int device, DeviceInfo* out);
@@ -49,16 +49,10 @@ long long sample_tiles(long long nvec, int cluster);
 cudaError_t launch_greedy(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
-// The sampling kernel that stages row slices in shared memory (16-byte
-// aligned rows whose slices fit); launch_sample dispatches to it.
-int sample_smem_cluster(long long nvec);
-cudaError_t sample_smem_prepare();
-cudaError_t launch_sample_smem(const VerifyArgs& a, int C, cudaStream_t stream);
-
-// The two-kernel sampling path (normaliser stream, then decide and sample).
-int sample_2p_cluster(long long nvec);
-cudaError_t sample_2p_prepare(int* stream_ctas_per_sm);
-cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
-                             cudaStream_t stream);
+// The fused sampling kernel (16-byte aligned rows of at most
+// kFusedMaxVec vectors); launch_sample dispatches to it.
+constexpr long long kFusedMaxVec = 65536;
+cudaError_t sample_fused_prepare();
+cudaError_t launch_sample_fused(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace specv

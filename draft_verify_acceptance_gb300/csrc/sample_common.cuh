@@ -95,6 +95,58 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   return v;
 }
 
+// Exact warp-wide sum of fixed-point masses below 2^59 with three 32-bit
+// reductions (redux.sync): the 22-bit limbs of 32 lanes sum below 2^27, so
+// no limb carries out.
+__device__ __forceinline__ unsigned long long warp_sum_mass(unsigned long long v) {
+  const unsigned int l0 = static_cast<unsigned int>(v & 0x3fffffull);
+  const unsigned int l1 = static_cast<unsigned int>((v >> 22) & 0x3fffffull);
+  const unsigned int l2 = static_cast<unsigned int>(v >> 44);
+  const unsigned long long s0 = __reduce_add_sync(0xffffffffu, l0);
+  const unsigned long long s1 = __reduce_add_sync(0xffffffffu, l1);
+  const unsigned long long s2 = __reduce_add_sync(0xffffffffu, l2);
+  return s0 + (s1 << 22) + (s2 << 44);
+}
+
+// Inclusive prefix sum over the lanes of a warp.
+__device__ __forceinline__ unsigned long long warp_scan_u64(unsigned long long v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
+// The element of a vector at which the fixed-point residual CDF passes
+// `rem` (the draw's threshold minus the mass before the vector): the running
+// fp32 sum of r in element order, rounded to fixed point exactly as the
+// vector's mass w was, so the last element's value equals w > rem and the
+// search always ends inside the vector.  c_prev / c_cur are the in-vector
+// CDF values just below and at the chosen element.
+template <int VEC>
+__device__ __forceinline__ int pick_in_vector(const float (&r)[VEC], unsigned long long w,
+                                              unsigned long long rem,
+                                              unsigned long long& c_prev,
+                                              unsigned long long& c_cur) {
+  float acc = 0.f;
+  int mstar = VEC - 1;
+  c_prev = 0;
+  c_cur = w;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) {
+    acc = __fadd_rn(acc, r[k]);
+    const unsigned long long cc = __float2ull_rn(__fmul_rn(acc, kFix));
+    if (cc > rem) {
+      mstar = k;
+      c_cur = cc;
+      break;
+    }
+    c_prev = cc;
+  }
+  return mstar;
+}
+
 // 16-byte staged vectors: unpacking and a NaN-ignoring running maximum.
 template <typename E>
 struct Staged;
@@ -134,6 +186,53 @@ struct Staged<F32> {
     x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
   }
 };
+
+// Online normaliser of one row relative to a scaled offset: the row's terms
+// are 2^(x*s - ms), summed in z.
+struct RowAcc {
+  float ms, z;
+};
+
+// Fold up to two 16-byte vectors held in registers into a row accumulator
+// without branches (so independent rows of a stage interleave): the new
+// offset is the larger of the old one and the vectors' packed maximum, the
+// old sum is rescaled by 2^(old - new) (exactly 1 when unchanged), and each
+// logit adds 2^(x*s - new) with one FFMA + ex2, summed as a tree.  An
+// accumulator that has seen no finite logit stays at (-inf, 0).  kFull: both
+// vectors are valid (nvalid == 2), so there are no per-element selects.
+template <typename E, bool kFull>
+__device__ __forceinline__ void acc_vectors_impl(RowAcc& A, const uint4 (&w)[2], int nvalid, float s) {
+  constexpr int VEC = Staged<E>::kVec;
+  typename Staged<E>::Max pm = Staged<E>::max_init();
+  if (kFull || nvalid > 0) Staged<E>::max_update(pm, w[0]);
+  if (kFull || nvalid > 1) Staged<E>::max_update(pm, w[1]);
+  const float nm = fmaxf(A.ms, Staged<E>::max_value(pm) * s);
+  const float f = (A.ms == nm) ? 1.f : ex2(A.ms - nm);
+  float e[2 * VEC];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float x[VEC];
+    Staged<E>::unpack(w[j], x);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k)
+      e[j * VEC + k] = (kFull || j < nvalid) ? ex2(fmaf(x[k], s, -nm)) : 0.f;
+  }
+#pragma unroll
+  for (int h = VEC; h > 0; h >>= 1)
+#pragma unroll
+    for (int k = 0; k < h; ++k) e[k] += e[k + h];
+  const float zn = fmaf(A.z, f, e[0]);
+  A.z = (nm == -INFINITY) ? 0.f : zn;
+  A.ms = nm;
+}
+template <typename E>
+__device__ __forceinline__ void acc_vectors(RowAcc& A, const uint4 (&w)[2], int nvalid, float s) {
+  acc_vectors_impl<E, false>(A, w, nvalid, s);
+}
+template <typename E>
+__device__ __forceinline__ void acc_vectors_full(RowAcc& A, const uint4 (&w)[2], float s) {
+  acc_vectors_impl<E, true>(A, w, 2, s);
+}
 
 // One element of a staged slice.
 template <typename E>

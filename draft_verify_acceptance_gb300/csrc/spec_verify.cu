@@ -29,8 +29,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess) e = greedy_occupancy(&d.greedy_ctas_per_sm);
     if (e == cudaSuccess) e = sample_prepare();
-    if (e == cudaSuccess) e = sample_smem_prepare();
-    if (e == cudaSuccess) e = sample_2p_prepare(&d.stream_ctas_per_sm);
+    if (e == cudaSuccess) e = sample_fused_prepare();
     g_info[device] = d;
     g_err[device] = e;
   });
@@ -52,7 +51,7 @@ size_t spec_verify_workspace_size(int B, int K, int V, int dtype, int mode) {
   if (B < 0 || K < 0 || K > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return 0;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return 0;
   if (mode != SPEC_MODE_SAMPLE && mode != SPEC_MODE_GREEDY) return 0;
-  return specv::workspace_bytes(B, K);
+  return specv::workspace_bytes(B, K, V, dtype == SPEC_DTYPE_BF16 ? 2 : 4);
 }
 
 spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits,
@@ -84,7 +83,7 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   if ((p_at_draft && !aligned(p_at_draft, 4)) || (q_at_draft && !aligned(q_at_draft, 4)) ||
       (flags && !aligned(flags, 4)) || (device_status && !aligned(device_status, 4)))
     return SPEC_ERR_INVALID_ARG;
-  const size_t need = specv::workspace_bytes(B, K);
+  const size_t need = specv::workspace_bytes(B, K, V, esz);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return SPEC_ERR_INVALID_ARG;
 
   // ---- launch ------------------------------------------------------------
@@ -111,15 +110,16 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   a.q_at = sample ? q_at_draft : nullptr;
   a.flags = flags;
   a.status = device_status;
-  const specv::WorkspaceLayout lay = specv::workspace_layout(B, K);
+  const specv::WorkspaceLayout lay = specv::workspace_layout(B, K, V, esz);
   a.seq = reinterpret_cast<specv::SeqState*>(static_cast<char*>(workspace) + lay.seq);
-  a.slots = static_cast<char*>(workspace) + lay.slots;
-  a.partials = static_cast<char*>(workspace) + lay.partials;
-  a.gathers = static_cast<char*>(workspace) + lay.gathers;
+  a.slots = static_cast<char*>(workspace) + lay.units;
+  a.partials = static_cast<char*>(workspace) + lay.units;
+  a.ctl = static_cast<char*>(workspace) + lay.ctl;
 
   const long long rows = static_cast<long long>(B) * (K + 1);
   if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
-  if (sample) {
+  const bool fused = a.vec && rowbytes / 16 <= specv::kFusedMaxVec;
+  if (sample && !fused) {  // limits of the streaming sampler
     const long long nvec = a.vec ? rowbytes / 16 : V;
     const int C = specv::sample_cluster_size(V, esz);
     if (specv::sample_tiles(nvec, C) > specv::kMaxTiles) return SPEC_ERR_UNSUPPORTED;

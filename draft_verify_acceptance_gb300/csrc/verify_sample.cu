@@ -407,12 +407,10 @@ cudaError_t sample_prepare() {
 cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   if (a.vec) {
     const long long nvec = static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16;
-    const int C2 = sample_2p_cluster(nvec);
-    if (C2 > 0) return launch_sample_2p(a, dev, C2, stream);
-    const int C = sample_smem_cluster(nvec);
-    if (C > 0) return launch_sample_smem(a, C, stream);
+    if (nvec <= kFusedMaxVec) return launch_sample_fused(a, dev, stream);
   }
-  // unaligned rows, or rows too long to stage: the streaming kernel below
+  // unaligned rows, or rows too long for the fused kernel: the streaming
+  // kernel below
   if (a.bf16) {
     return a.vec ? launch_sample_t<BF16, 8, 4>(a, stream)
                  : launch_sample_t<BF16, 1, 8>(a, stream);

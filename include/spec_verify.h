@@ -84,8 +84,10 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 
 /*
  * Bytes of workspace a call with these sizes needs (a multiple of 256).
- * The workspace holds per-sequence arrival counters, reject masks and
- * per-row candidates.  It MUST be zero-filled before its first use; every
+ * The workspace holds per-sequence arrival counters, per-row candidates or
+ * per-work-unit softmax partials (one unit is a segment of 2048 16-byte
+ * vectors of a target row and its draft row), and two work counters; its
+ * size grows with B, K and V * element size.  It MUST be zero-filled before its first use; every
  * call that returns SPEC_OK leaves it zero-filled again when the kernel
  * completes, so it can be reused by later calls on the same stream without
  * clearing.  One workspace serves one call at a time: calls that may overlap
@@ -173,9 +175,9 @@ SPEC_API spec_status_t spec_verify_ex(const void* target_logits, const void* dra
  * exits.
  *
  *   - The batch must fit: spec_verify_workspace_size(B, K, V, dtype, mode) must
- *     not exceed SPEC_STATIC_SCRATCH_BYTES (for example B = 1024 with K = 16,
- *     or B = 4096 with K = 4), else SPEC_ERR_SCRATCH_LIMIT and nothing is
- *     queued.  Other argument errors are those of spec_verify.
+ *     not exceed SPEC_STATIC_SCRATCH_BYTES (at V = 32000 bf16, for example,
+ *     B = 1024 with K = 16 or B = 4096 with K = 4 fit), else
+ *     SPEC_ERR_SCRATCH_LIMIT and nothing is queued.  Other argument errors are those of spec_verify.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress, with the device current) and does the
  *     library's one-time kernel set-up; make that first call before any stream
