@@ -71,13 +71,20 @@ struct __align__(16) FusedCtl {
   unsigned long long done_ctas;  // CTAs that have taken their last unit
 };
 
-// Workspace layout: SeqState[B] | units | FusedCtl, 16-byte aligned parts,
-// where `units` is either RowSlot[B*(K+1)] (greedy kernel, streaming sampler)
-// or Partial[B * tasks_per_seq] (fused sampler).  One call uses one of the
-// two views and leaves the region zero-filled, so both views can share it.
-// The size is taken for 16-byte vectors of the row (ceil(V*bytes/16)).
+// Largest persistent grid of the two-kernel sampler's streaming pass.  Its
+// partials need at most kMaxStreamCtas + rows slots (contributor c of row pair
+// p writes slot c + p).
+constexpr long long kMaxStreamCtas = 4096;
+
+// Workspace layout: SeqState[B] | units | float2 gathers[B*(K+1)] | FusedCtl,
+// 16-byte aligned parts, where `units` is RowSlot[B*(K+1)] (greedy kernel,
+// streaming sampler), Partial[B * tasks_per_seq] (fused sampler) or
+// Partial[kMaxStreamCtas + B*(K+1) + 1] (two-kernel sampler, which also uses
+// the gathers).  One call uses one view and leaves everything zero-filled,
+// so the views can share the region.  Sizes use 16-byte vectors of the row
+// (ceil(V*bytes/16)).
 struct WorkspaceLayout {
-  size_t seq, units, ctl, total;
+  size_t seq, units, gathers, ctl, total;
 };
 inline WorkspaceLayout workspace_layout(long long B, long long K, long long V, int elem_bytes) {
   const size_t R = (size_t)B * (size_t)(K + 1);
@@ -86,9 +93,11 @@ inline WorkspaceLayout workspace_layout(long long B, long long K, long long V, i
   WorkspaceLayout l;
   l.seq = 0;
   l.units = l.seq + (size_t)B * sizeof(SeqState);
-  const size_t ub = (R * sizeof(RowSlot) > P * sizeof(Partial)) ? R * sizeof(RowSlot)
-                                                                : P * sizeof(Partial);
-  l.ctl = l.units + ub;
+  size_t ub = R * sizeof(RowSlot);
+  if (P * sizeof(Partial) > ub) ub = P * sizeof(Partial);
+  if (((size_t)kMaxStreamCtas + R + 1) * sizeof(Partial) > ub) ub = ((size_t)kMaxStreamCtas + R + 1) * sizeof(Partial);
+  l.gathers = l.units + ub;
+  l.ctl = (l.gathers + R * 8 + 15) & ~(size_t)15;
   l.total = ((l.ctl + sizeof(FusedCtl)) + 255) & ~(size_t)255;
   return l;
 }

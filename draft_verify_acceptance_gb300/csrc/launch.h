@@ -31,12 +31,14 @@ struct VerifyArgs {
   void* partials;              // workspace: Partial per work unit (fused sampler); same
                                // region as `slots`
   void* ctl;                   // workspace: FusedCtl
+  void* gathers;               // workspace: [B*(K+1)] float2 (two-kernel sampler)
 };
 
 // Per-device facts gathered once.
 struct DeviceInfo {
   int sm_count = 0;
   int greedy_ctas_per_sm = 0;  // occupancy of the greedy kernel
+  int stream_ctas_per_sm = 0;  // occupancy of the two-kernel sampler's streaming pass
 };
 
 cudaError_t device_info(int device, DeviceInfo* out);
@@ -54,5 +56,12 @@ cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream
 constexpr long long kFusedMaxVec = 65536;
 cudaError_t sample_fused_prepare();
 cudaError_t launch_sample_fused(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// The two-kernel sampler (normaliser stream, then decide and draw with one
+// cluster per sequence) for rows whose draw spans several draw segments.
+int sample_2p_cluster(long long nvec);
+cudaError_t sample_2p_prepare(int* stream_ctas_per_sm);
+cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
+                             cudaStream_t stream);
 
 }  // namespace specv

@@ -30,6 +30,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     if (e == cudaSuccess) e = greedy_occupancy(&d.greedy_ctas_per_sm);
     if (e == cudaSuccess) e = sample_prepare();
     if (e == cudaSuccess) e = sample_fused_prepare();
+    if (e == cudaSuccess) e = sample_2p_prepare(&d.stream_ctas_per_sm);
     g_info[device] = d;
     g_err[device] = e;
   });
@@ -115,6 +116,7 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   a.slots = static_cast<char*>(workspace) + lay.units;
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
+  a.gathers = static_cast<char*>(workspace) + lay.gathers;
 
   const long long rows = static_cast<long long>(B) * (K + 1);
   if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;

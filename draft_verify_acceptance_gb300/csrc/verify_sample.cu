@@ -407,6 +407,12 @@ cudaError_t sample_prepare() {
 cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   if (a.vec) {
     const long long nvec = static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16;
+    // a draw that fits one segment: the fused kernel draws as it streams;
+    // longer rows: the two-kernel sampler, whose per-sequence clusters finish
+    // the last draws sooner
+    if (nvec <= kFusedSeg) return launch_sample_fused(a, dev, stream);
+    const int C = sample_2p_cluster(nvec);
+    if (C > 0) return launch_sample_2p(a, dev, C, stream);
     if (nvec <= kFusedMaxVec) return launch_sample_fused(a, dev, stream);
   }
   // unaligned rows, or rows too long for the fused kernel: the streaming

@@ -1,0 +1,690 @@
+// verify_sample_2p.cu -- speculative-sampling verification on sm_103a in two
+// kernels with no cross-CTA atomics on either critical path.
+//
+// Sources (page title, section):
+//   "推测性拒绝采样", 技术原理与步骤 steps 2-4: the target's K+1 rows come from
+//     one parallel pass; x_i is accepted when p(x_i) >= q(x_i), else with
+//     probability p(x_i)/q(x_i); everything after the first rejection is
+//     dropped and one replacement token is drawn there.  关键保证: the output
+//     follows the target distribution exactly, which makes the replacement
+//     law normalize(max(0, p - q)).
+//   "논문 리뷰 [Speculative Contrastive Decoding]", Speculative Decoding: with
+//     all K accepted, the target supplies token K+1 (drawn from p_K).
+//
+// Kernel A (normaliser stream): a persistent grid of G CTAs streams every
+// (target row i, draft row i) pair once from HBM through a ring of shared-
+// memory stages filled by cp.async.bulk.  The pairs, position-major, form one
+// flat space of 16-byte vectors weighted by their bytes (32 per draft pair
+// vector, 16 per bonus-row vector); CTA c owns a byte-balanced contiguous
+// range of it.  Each thread keeps online normalisers of both rows relative to
+// scaled offsets; at a row change the warps fold them into shared memory, and
+// at the end warp 0 writes one Partial per (CTA, pair) to slot c + pair -- a
+// plain store.  The CTA that streams the vector holding x_i stores t[x_i] and
+// d[x_i].
+// Kernel B (decide and sample), launched as a programmatic dependent of A:
+// one cluster per sequence.  Warp 0 of rank 0 merges each row's partials in
+// contributor order, runs the K accept tests in parallel lanes and finds the
+// first rejection n with a ballot; every CTA of the cluster then stages its
+// slice of row pair n (or of the bonus row) with one bulk copy and the
+// fixed-point inverse CDF of the staged kernel picks the token.  Rank 0
+// writes the outputs.  Kernel B re-reads about one row pair per sequence.
+#include <cooperative_groups.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "sample_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace specv {
+
+// Byte-weighted partition of the pair-vector space over G CTAs.  Vectors
+// [0, P) belong to draft pairs (positions 0..K-1, weight 2), [P, P + Q) to
+// bonus rows (position K, weight 1); pair p = i*B + b covers vectors
+// [p*nvec, (p+1)*nvec).
+struct StreamPartition {
+  long long nvec, P, Q, W;
+  int G;
+  __host__ __device__ long long vec_of_w(long long w) const {
+    return w <= 2 * P ? w / 2 : P + (w - 2 * P);
+  }
+  __host__ __device__ long long w_of_vec(long long v) const {
+    return v <= P ? 2 * v : 2 * P + (v - P);
+  }
+  // first vector of CTA c (c = G gives the end)
+  __host__ __device__ long long lo(int c) const {
+    return c >= G ? P + Q : vec_of_w(W * c / G);
+  }
+  // the CTA whose range holds vector v: the largest c with lo(c) <= v
+  __host__ __device__ int cta_of(long long v) const {
+    const long long c = (w_of_vec(v + 1) * G - 1) / W;
+    return static_cast<int>(c < G - 1 ? c : G - 1);
+  }
+};
+
+namespace {
+
+constexpr int kStages2 = 4;
+constexpr int kChunk2 = 512;              // vectors per row per stage (8 KiB)
+constexpr int kProducer2 = kThreads - 32;  // issues kernel B's bulk copies
+constexpr int kMaxPending2 = 32;
+
+// Walks [pos, hi) in chunks of at most kChunk2 vectors that never cross a
+// pair; the pair and its (position i, sequence b) are tracked incrementally,
+// so the loop has no division.
+struct PairCursor {
+  long long pos, hi, nvec, pair_end;
+  int i, b, B;
+  __device__ PairCursor(long long lo, long long hi_, long long nvec_, int B_)
+      : pos(lo), hi(hi_), nvec(nvec_), B(B_) {
+    const long long p = lo / nvec_;
+    pair_end = (p + 1) * nvec_;
+    i = static_cast<int>(p / B_);
+    b = static_cast<int>(p - static_cast<long long>(i) * B_);
+  }
+  // next chunk: start, length, the pair's (i, b) and the offset in the pair.
+  // A chunk of a draft pair holds kChunk2 vectors of each row; a chunk of a
+  // bonus row (i == K, target only) holds 2 * kChunk2, so every stage carries
+  // the same bytes and the byte-balanced partition balances chunks too.
+  __device__ bool next(long long& start, int& len, int& pi, int& pb, long long& off, int K) {
+    if (pos >= hi) return false;
+    if (pos >= pair_end) {
+      pair_end += nvec;
+      if (++b == B) {
+        b = 0;
+        ++i;
+      }
+    }
+    long long end = pos + (i < K ? kChunk2 : 2 * kChunk2);
+    if (end > hi) end = hi;
+    if (end > pair_end) end = pair_end;
+    start = pos;
+    len = static_cast<int>(end - pos);
+    pi = i;
+    pb = b;
+    off = pos - (pair_end - nvec);
+    pos = end;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void issue_chunk(const VerifyArgs& a, long long nvec, int i, int b,
+                                           long long off, int len, uint4* stage,
+                                           unsigned long long* bar) {
+  const uint32_t bytes = static_cast<uint32_t>(len) * 16u;
+  const uint4* trow = static_cast<const uint4*>(a.target) +
+                      (static_cast<size_t>(b) * (a.K + 1) + i) * nvec + off;
+  if (i < a.K) {
+    const uint4* drow = static_cast<const uint4*>(a.draft) +
+                        (static_cast<size_t>(b) * a.K + i) * nvec + off;
+    mbar_arrive_expect_tx(bar, 2u * bytes);
+    bulk_load(stage, trow, bytes, bar);
+    bulk_load(stage + kChunk2, drow, bytes, bar);
+  } else {
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(stage, trow, bytes, bar);
+  }
+}
+
+// The draft token of pair (i, b) (clamped into the vocabulary), or -1 for a
+// bonus row or past the end.
+__device__ __forceinline__ int pair_token(const VerifyArgs& a, int i, int b) {
+  if (i >= a.K) return -1;
+  const int x = __ldg(a.tokens + static_cast<size_t>(b) * a.K + i);
+  return min(max(x, 0), a.V - 1);
+}
+
+constexpr int kThreadsA = kThreads + 32;  // 8 consumer warps + 1 producer warp
+
+// Consumer warps only (named barrier 1): warp 0 merges the parked partials of
+// each pair over the 8 warps and stores one Partial per (CTA, pair).
+__device__ __forceinline__ void flush_partials(Partial* partials, int c, const float4* s_pend,
+                                               const long long* s_pair, int npend, int warp,
+                                               int lane) {
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+  if (warp == 0) {
+    for (int j = lane; j < npend; j += 32) {
+      float4 v = s_pend[j * kWarps];
+      for (int w = 1; w < kWarps; ++w) {
+        const float4 u = s_pend[j * kWarps + w];
+        merge_scaled(v.x, v.y, u.x, u.y);
+        merge_scaled(v.z, v.w, u.z, u.w);
+      }
+      Partial out;
+      out.ms_t = v.x; out.z_t = v.y; out.ms_d = v.z; out.z_d = v.w;
+      partials[c + s_pair[j]] = out;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+static_assert(kChunk2 == 2 * kThreads, "two vectors per consumer thread per row and stage");
+
+template <typename E>
+__global__ void __launch_bounds__(kThreadsA)
+norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
+  constexpr int VEC = Staged<E>::kVec;
+  extern __shared__ __align__(128) uint4 ring2[];  // [kStages2][target, draft][kChunk2]
+  __shared__ __align__(8) unsigned long long full[kStages2];   // copies landed
+  __shared__ __align__(8) unsigned long long empty[kStages2];  // consumers done
+  __shared__ long long s_pair[kMaxPending2];
+  __shared__ float4 s_pend[kMaxPending2 * kWarps];
+
+  // the decide-and-sample kernel may be scheduled as soon as SMs free up;
+  // it waits for this grid's results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const int c = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long nvec = pt.nvec;
+  const long long vlo = pt.lo(c), vhi = pt.lo(c + 1);
+  const float s = a.scale;
+
+  if (tid == 0) {
+    for (int q = 0; q < kStages2; ++q) {
+      mbar_init(&full[q], 1);
+      mbar_init(&empty[q], kWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // ---- producer warp: one thread keeps kStages2 chunks in flight ---------
+  if (warp == kWarps) {
+    if (lane == 0) {
+      PairCursor prod(vlo, vhi, nvec, a.B);
+      bool ok = true;
+      long long st, off;
+      int len, pi, pb;
+      for (int k = 0; prod.next(st, len, pi, pb, off, a.K); ++k) {
+        const int q = k % kStages2;
+        if (k >= kStages2 && !mbar_wait_sleep(&empty[q], static_cast<uint32_t>((k / kStages2 - 1) & 1)))
+          ok = false;
+        issue_chunk(a, nvec, pi, pb, off, len, ring2 + static_cast<size_t>(q) * 2 * kChunk2, &full[q]);
+      }
+      if (!ok && a.status) atomicOr(a.status, kWaitTimeout);
+    }
+    return;
+  }
+
+  // ---- consumer warps -----------------------------------------------------
+  // Per-pair facts are set once per pair; per chunk only 32-bit arithmetic.
+  Partial* partials = static_cast<Partial*>(a.partials);
+  float2* gathers = static_cast<float2*>(a.gathers);
+  long long pos = vlo;
+  long long p = vlo / nvec;                 // current pair
+  long long pair_end = (p + 1) * nvec;      // its end in the flat space
+  int in_pair = static_cast<int>(vlo - p * nvec);  // vectors of the pair before pos
+  int ci = static_cast<int>(p / a.B);       // (position, sequence) of pair p
+  int cb = static_cast<int>(p - static_cast<long long>(ci) * a.B);
+  const int nb = cb + 1 == a.B ? 0 : cb + 1, ni = cb + 1 == a.B ? ci + 1 : ci;
+  int x_cur = pair_token(a, ci, cb);        // clamped token, or -1 for a bonus row
+  int x_nxt = pair_token(a, ni, nb);        // prefetched for the next pair
+  int npend = 0;
+  RowAcc At{-INFINITY, 0.f}, Ad{-INFINITY, 0.f};
+  bool ok = true;
+
+  for (int k = 0; pos < vhi; ++k) {
+    if (pos == pair_end) {  // pair change: park the finished pair's partial
+      float mt = At.ms, zt = At.z, md = Ad.ms, zd = Ad.z;
+      warp_merge_scaled(mt, zt);
+      warp_merge_scaled(md, zd);
+      if (lane == 0) s_pend[npend * kWarps + warp] = make_float4(mt, zt, md, zd);
+      if (tid == 0) s_pair[npend] = p;
+      if (++npend == kMaxPending2) {
+        flush_partials(partials, c, s_pend, s_pair, npend, warp, lane);
+        npend = 0;
+      }
+      ++p;
+      pair_end += nvec;
+      in_pair = 0;
+      if (++cb == a.B) {
+        cb = 0;
+        ++ci;
+      }
+      x_cur = x_nxt;
+      x_nxt = cb + 1 == a.B ? pair_token(a, ci + 1, 0) : pair_token(a, ci, cb + 1);
+      At = RowAcc{-INFINITY, 0.f};
+      Ad = RowAcc{-INFINITY, 0.f};
+    }
+    const bool has_draft = x_cur >= 0;
+    long long end = pos + (has_draft ? kChunk2 : 2 * kChunk2);
+    if (end > vhi) end = vhi;
+    if (end > pair_end) end = pair_end;
+    const int len = static_cast<int>(end - pos);
+    const int q = k % kStages2;
+    if (!mbar_wait_sleep(&full[q], static_cast<uint32_t>((k / kStages2) & 1))) ok = false;
+    const uint4* stage_t = ring2 + static_cast<size_t>(q) * 2 * kChunk2;
+    const uint4* stage_d = stage_t + kChunk2;
+    // draft pair: wt = target vectors, wd = draft vectors of the same range;
+    // bonus row: wt and wd are the two halves of a double-length target chunk
+    const int half = has_draft ? len : (len < kChunk2 ? len : kChunk2);
+    const int rest = has_draft ? len : len - half;
+    const int nvalid = (tid < half ? 1 : 0) + (tid + kThreads < half ? 1 : 0);
+    const int nvalid2 = (tid < rest ? 1 : 0) + (tid + kThreads < rest ? 1 : 0);
+    uint4 wt[2], wd[2];
+    if (nvalid > 0) wt[0] = stage_t[tid];
+    if (nvalid > 1) wt[1] = stage_t[tid + kThreads];
+    if (nvalid2 > 0) wd[0] = stage_d[tid];
+    if (nvalid2 > 1) wd[1] = stage_d[tid + kThreads];
+    if (has_draft) {
+      // the thread holding x_i's vector records t[x_i], d[x_i]
+      const int lv = x_cur / VEC - in_pair;
+      if (lv >= 0 && lv < len && (lv & (kThreads - 1)) == tid) {
+        const int j = lv * VEC + x_cur % VEC;
+        gathers[p] = make_float2(staged_elem<E>(stage_t, j), staged_elem<E>(stage_d, j));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[q]);  // this warp is done reading stage q
+    acc_vectors<E>(At, wt, nvalid, s);
+    acc_vectors<E>(has_draft ? Ad : At, wd, nvalid2, s);
+    pos = end;
+    in_pair += len;
+  }
+  {  // the last pair
+    float mt = At.ms, zt = At.z, md = Ad.ms, zd = Ad.z;
+    warp_merge_scaled(mt, zt);
+    warp_merge_scaled(md, zd);
+    if (lane == 0) s_pend[npend * kWarps + warp] = make_float4(mt, zt, md, zd);
+    if (tid == 0) s_pair[npend] = p;
+    ++npend;
+  }
+  flush_partials(partials, c, s_pend, s_pair, npend, warp, lane);
+  if (!ok && a.status) atomicOr(a.status, kWaitTimeout);
+}
+
+constexpr int kMaxCB = 8;                // largest cluster of kernel B
+constexpr int kSmemB3 = 72 * 1024;       // slice bytes for three CTAs per SM
+constexpr int kSmemBMax = 200 * 1024;    // slice bytes for one CTA per SM
+
+// Decision of one sequence, pushed from rank 0 to every CTA of its cluster.
+struct Decision {
+  float MSt, Zt, MSd, Zd;  // normalisers of the row pair that is drawn from
+  float uK;
+  int n;                   // number of accepted draft tokens
+  int ratio_near;          // a ratio test at a position <= n was within the band
+  int pad;
+};
+
+template <typename E>
+__global__ void __launch_bounds__(kThreads)
+decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
+  constexpr int VEC = Staged<E>::kVec;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int b = static_cast<int>(blockIdx.x / C);
+  const int K = a.K, K1 = K + 1;
+  const long long nvec = pt.nvec;
+  const float s = a.scale;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  extern __shared__ __align__(128) uint4 smem[];
+  uint4* st = smem;
+  uint4* sd = smem + nvs;
+  unsigned long long* tws = reinterpret_cast<unsigned long long*>(smem + 2 * static_cast<size_t>(nvs));
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ Decision s_dec;                           // this CTA's decision
+  __shared__ unsigned long long s_mass[2][kMaxCB];     // pushed by each rank
+  __shared__ int s_tok[2];                             // pushed by the crossing CTA to rank 0
+
+  cluster_arrive_relaxed();  // matched by cluster_wait() before the first DSMEM push
+  // everything below reads what the normaliser stream wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+
+  // ---- decision (warp 0 of every CTA; identical in all of them) ----------
+  // One lane per position: all loads first, then the merge in contributor
+  // order and the ratio test; a ballot gives the first rejection n.  Only
+  // rank 0 writes p(x_i), q(x_i) and the status.
+  if (warp == 0) {
+    const Partial* partials = static_cast<const Partial*>(a.partials);
+    const float2* gathers = static_cast<const float2*>(a.gathers);
+    const float* u = a.uniforms + static_cast<size_t>(b) * K1;
+    const bool writer = rank == 0;
+    int n = K, bad = 0, ratio_near = 0;
+    float nMSt = 0.f, nZt = 0.f, nMSd = 0.f, nZd = 0.f;
+    for (int i0 = 0; i0 < K1; i0 += 32) {
+      const int i = i0 + lane;
+      float MSt = -INFINITY, Zt = 0.f, MSd = -INFINITY, Zd = 0.f;
+      bool rej = false, nr = false;
+      if (i <= K) {
+        const long long p = static_cast<long long>(i) * a.B + b;
+        const int f = pt.cta_of(p * nvec), l = pt.cta_of((p + 1) * nvec - 1);
+        const int nc = l - f + 1;
+        Partial qa[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nc) qa[j] = partials[f + j + p];
+        float2 g = make_float2(0.f, 0.f);
+        int xr = 0;
+        if (i < K) {
+          g = gathers[p];
+          xr = a.tokens[static_cast<size_t>(b) * K + i];
+        }
+        const float ui = u[i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (j < nc) {
+            merge_scaled(MSt, Zt, qa[j].ms_t, qa[j].z_t);
+            merge_scaled(MSd, Zd, qa[j].ms_d, qa[j].z_d);
+          }
+        }
+        for (int j = 4; j < nc; ++j) {  // rows spread over many CTAs (small B*K)
+          const Partial q = partials[f + j + p];
+          merge_scaled(MSt, Zt, q.ms_t, q.z_t);
+          merge_scaled(MSd, Zd, q.ms_d, q.z_d);
+        }
+        if (!(isfinite(MSt) && isfinite(Zt) && Zt > 0.f)) bad |= kDataNonfiniteLogit;
+        if (!(ui >= 0.f && ui < 1.f)) bad |= kDataUniformRange;
+        if (i < K) {
+          if (xr < 0 || xr >= a.V) bad |= kDataTokenRange;
+          if (!(isfinite(MSd) && isfinite(Zd) && Zd > 0.f)) bad |= kDataNonfiniteLogit;
+          const float px = ex2(fmaf(g.x, s, -MSt)) / Zt;
+          const float qx = ex2(fmaf(g.y, s, -MSd)) / Zd;
+          if (writer && a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
+          if (writer && a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
+          rej = !(ui * qx < px);
+          nr = qx > 0.f && fabsf(ui - fminf(1.f, px / qx)) < kBandF;
+        }
+      }
+      const unsigned rb = __ballot_sync(0xffffffffu, rej);
+      const unsigned nb = __ballot_sync(0xffffffffu, nr);
+      if (n == K) {  // still no rejection before this round (warp-uniform)
+        int pick = -1;
+        if (rb) {
+          pick = __ffs(rb) - 1;
+          n = i0 + pick;
+          ratio_near |= (nb & (pick == 31 ? 0xffffffffu : ((2u << pick) - 1u))) != 0u;
+        } else {
+          ratio_near |= nb != 0u;
+          if (K - i0 < 32) pick = K - i0;  // the bonus row is in this round
+        }
+        if (pick >= 0) {
+          nMSt = __shfl_sync(0xffffffffu, MSt, pick);
+          nZt = __shfl_sync(0xffffffffu, Zt, pick);
+          nMSd = __shfl_sync(0xffffffffu, MSd, pick);
+          nZd = __shfl_sync(0xffffffffu, Zd, pick);
+        }
+      }
+    }
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      if (writer && bad && a.status) atomicOr(a.status, bad);
+      Decision d;
+      d.MSt = nMSt; d.Zt = nZt; d.MSd = nMSd; d.Zd = nZd;
+      d.uK = u[K];
+      d.n = n;
+      d.ratio_near = ratio_near;
+      d.pad = 0;
+      s_dec = d;
+    }
+  }
+  __syncthreads();
+
+  // ---- stage this CTA's slice of row pair n (or of the bonus row) --------
+  const Decision dec = s_dec;
+  const int n = dec.n;
+  bool residual = n < K;
+  const long long v0 = nvec * rank / C;
+  const int nv = static_cast<int>(nvec * (rank + 1) / C - v0);
+  const int ntl = (nv + kThreads - 1) / kThreads;
+  if (tid == kProducer2) {
+    const uint32_t bytes = static_cast<uint32_t>(nv) * 16u;
+    const uint4* trow = static_cast<const uint4*>(a.target) + (static_cast<size_t>(b) * K1 + n) * nvec + v0;
+    mbar_arrive_expect_tx(&bar, residual ? 2u * bytes : bytes);
+    bulk_load(st, trow, bytes, &bar);
+    if (residual)
+      bulk_load(sd, static_cast<const uint4*>(a.draft) + (static_cast<size_t>(b) * K + n) * nvec + v0,
+                bytes, &bar);
+  }
+  if (tid == 0 && !mbar_wait_one(&bar, 0) && !mbar_wait_one(&bar, 0) && a.status)
+    atomicOr(a.status, kWaitTimeout);
+  __syncthreads();
+
+  cluster_wait();  // every CTA of the cluster has started
+  // ---- pass 2: fixed-point mass of the staged slice ----------------------
+  const float MSt = dec.MSt, MSd = dec.MSd;
+  const float invZt = 1.f / dec.Zt;
+  const float invZd = residual ? 1.f / dec.Zd : 0.f;
+  int rnd = 0;
+  unsigned long long S = 0;
+  for (;; ++rnd) {
+    for (int k = 0; k < ntl; ++k) {
+      const int v = k * kThreads + tid;
+      float xt[VEC], xd[VEC], r[VEC];
+      if (v < nv) {
+        Staged<E>::unpack(st[v], xt);
+        if (residual) Staged<E>::unpack(sd[v], xd);
+      } else {
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) xt[q] = xd[q] = -INFINITY;
+      }
+      const unsigned long long w =
+          warp_sum_u64(vec_weight_scaled<VEC>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r));
+      if (lane == 0) tws[k * kWarps + warp] = w;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long t = 0;
+      for (int k = lane; k < ntl * kWarps; k += 32) t += tws[k];
+      t = warp_sum_u64(t);
+      if (lane < C) *cluster.map_shared_rank(&s_mass[rnd][rank], lane) = t;
+    }
+    cluster.sync();
+    S = 0;
+    for (int r = 0; r < C; ++r) S += s_mass[rnd][r];
+    if (S != 0 || !residual || rnd == 1) break;
+    residual = false;  // p == q at this row: the draw falls back to p
+  }
+
+  // every CTA of the cluster has read the partials and gathers (they were
+  // read before the slice was staged): rank 0 puts its sequence's slots back
+  // to zero, keeping the workspace zero-filled between calls
+  if (rank == 0 && warp == 0) {
+    Partial* partials = static_cast<Partial*>(a.partials);
+    float2* gathers = static_cast<float2*>(a.gathers);
+    for (int i = lane; i <= K; i += 32) {
+      const long long p = static_cast<long long>(i) * a.B + b;
+      const int f = pt.cta_of(p * nvec), l = pt.cta_of((p + 1) * nvec - 1);
+      for (int c = f; c <= l; ++c) partials[c + p] = Partial{0.f, 0.f, 0.f, 0.f};
+      if (i < K) gathers[p] = make_float2(0.f, 0.f);
+    }
+  }
+
+  int token = 0, near = 0;
+  if (S != 0) {
+    double th = static_cast<double>(dec.uK) * static_cast<double>(S);
+    if (!(th >= 0.0)) th = 0.0;
+    const unsigned long long theta =
+        (th >= static_cast<double>(S)) ? S - 1 : static_cast<unsigned long long>(th);
+    int cstar = C - 1;
+    unsigned long long off = 0;
+    for (int r = 0; r < C; ++r) {
+      const unsigned long long m = s_mass[rnd][r];
+      if (off + m > theta) { cstar = r; break; }
+      off += m;
+    }
+    // ---- pass 3: the crossing inside the slice of rank cstar (warp 0) ----
+    if (rank == cstar && warp == 0 && ntl > 0) {
+      const unsigned long long tl = theta - off;
+      unsigned long long base = 0;
+      int kstar = ntl - 1;
+      for (int k0 = 0; k0 < ntl; k0 += 32) {
+        const int k = k0 + lane;
+        unsigned long long tt = 0;
+        if (k < ntl)
+          for (int w = 0; w < kWarps; ++w) tt += tws[k * kWarps + w];
+        unsigned long long incl = tt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += o;
+        }
+        const unsigned int hit = __ballot_sync(0xffffffffu, k < ntl && base + incl > tl);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          base += __shfl_sync(0xffffffffu, incl - tt, l);
+          kstar = k0 + l;
+          break;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      int wstar = kWarps - 1;
+      for (int w = 0; w < kWarps; ++w) {
+        const unsigned long long m = tws[kstar * kWarps + w];
+        if (base + m > tl) { wstar = w; break; }
+        base += m;
+      }
+      const int v = kstar * kThreads + wstar * 32 + lane;
+      float xt[VEC], xd[VEC], r[VEC];
+      if (v < nv) {
+        Staged<E>::unpack(st[v], xt);
+        if (residual) Staged<E>::unpack(sd[v], xd);
+      } else {
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) xt[q] = xd[q] = -INFINITY;
+      }
+      const unsigned long long w = vec_weight_scaled<VEC>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r);
+      unsigned long long incl = w;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+      }
+      const unsigned int hit = __ballot_sync(0xffffffffu, base + incl > tl);
+      const int lstar = hit ? (__ffs(hit) - 1) : 31;
+      if (lane == lstar) {
+        const unsigned long long before = base + incl - w;
+        const unsigned long long rem = tl - before;
+        float acc = 0.f;
+        int mstar = VEC - 1;
+        unsigned long long c_prev = 0, c_cur = w;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+          acc = __fadd_rn(acc, r[k]);
+          const unsigned long long cc = __float2ull_rn(__fmul_rn(acc, kFix));
+          if (cc > rem) { mstar = k; c_cur = cc; break; }
+          c_prev = cc;
+        }
+        const long long t = (v0 + v) * VEC + mstar;
+        const double band = 1e-6 * static_cast<double>(S);
+        const bool nr = fabs(th - static_cast<double>(off + before + c_prev)) < band ||
+                        fabs(static_cast<double>(off + before + c_cur) - th) < band;
+        int* dst = cluster.map_shared_rank(&s_tok[0], 0);
+        dst[0] = static_cast<int>(t < a.V ? t : a.V - 1);
+        dst[1] = nr ? 1 : 0;
+      }
+    }
+    cluster.sync();  // the token has reached rank 0
+    token = s_tok[0];
+    near = s_tok[1];
+  }
+
+  // ---- outputs (warp 0 of rank 0) ----------------------------------------
+  if (rank == 0 && warp == 0) {
+    const int32_t* x = a.tokens + static_cast<size_t>(b) * K;
+    int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
+    for (int j = lane; j < K1; j += 32)
+      out[j] = (j < n) ? min(max(x[j], 0), a.V - 1) : (j == n ? token : -1);
+    if (lane == 0) {
+      a.accepted_len[b] = n;
+      if (a.flags) a.flags[b] = (dec.ratio_near ? kFlagRatio : 0u) | (near ? kFlagCdf : 0u);
+    }
+  }
+}
+
+size_t smem_b(long long nvec, int C) {
+  const long long nvs = (nvec + C - 1) / C;
+  const long long ntiles = (nvs + kThreads - 1) / kThreads;
+  return static_cast<size_t>(2 * nvs * 16 + ntiles * kWarps * 8);
+}
+
+constexpr int kSmemA = kStages2 * 2 * kChunk2 * 16;
+
+}  // namespace
+
+// Cluster size of kernel B: the smallest C in {1, 2, 4, 8} whose slices fit
+// three CTAs per SM, else 8 if they fit one CTA per SM, else 0 (the rows are
+// too long for this path).
+int sample_2p_cluster(long long nvec) {
+  for (int C = 1; C <= kMaxCB; C *= 2)
+    if (smem_b(nvec, C) <= static_cast<size_t>(kSmemB3)) return C;
+  return smem_b(nvec, kMaxCB) <= static_cast<size_t>(kSmemBMax) ? kMaxCB : 0;
+}
+
+cudaError_t sample_2p_prepare(int* stream_ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(norm_stream_kernel<BF16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemA);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(norm_stream_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemA);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decide_sample_kernel<BF16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBMax);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decide_sample_kernel<F32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBMax);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(stream_ctas_per_sm, norm_stream_kernel<BF16>,
+                                                      kThreadsA, kSmemA);
+  return e;
+}
+
+StreamPartition stream_partition(const VerifyArgs& a, const DeviceInfo& dev) {
+  StreamPartition pt;
+  pt.nvec = static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16;
+  pt.P = static_cast<long long>(a.K) * a.B * pt.nvec;
+  pt.Q = static_cast<long long>(a.B) * pt.nvec;
+  pt.W = 2 * pt.P + pt.Q;
+  // two CTAs per SM: 8 stages of 16 KiB in flight per SM, and room to compute
+  const int per_sm = dev.stream_ctas_per_sm < 2 ? (dev.stream_ctas_per_sm > 0 ? dev.stream_ctas_per_sm : 1) : 2;
+  long long G = static_cast<long long>(dev.sm_count) * per_sm;
+  if (G > kMaxStreamCtas) G = kMaxStreamCtas;
+  if (G > pt.W / 4) G = pt.W / 4;  // every CTA owns at least one vector
+  if (G < 1) G = 1;
+  pt.G = static_cast<int>(G);
+  return pt;
+}
+
+cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
+                             cudaStream_t stream) {
+  const StreamPartition pt = stream_partition(a, dev);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned int>(pt.G));
+    cfg.blockDim = dim3(kThreadsA);
+    cfg.dynamicSmemBytes = kSmemA;
+    cfg.stream = stream;
+    const cudaError_t e = a.bf16 ? cudaLaunchKernelEx(&cfg, norm_stream_kernel<BF16>, a, pt)
+                                 : cudaLaunchKernelEx(&cfg, norm_stream_kernel<F32>, a, pt);
+    if (e != cudaSuccess) return e;
+  }
+  const long long grid = static_cast<long long>(a.B) * C;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  const int nvs = static_cast<int>((pt.nvec + C - 1) / C);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned int>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_b(pt.nvec, C);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16>, a, pt, nvs)
+                : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32>, a, pt, nvs);
+}
+
+}  // namespace specv
