@@ -327,16 +327,12 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* p, un
 }
 
 // ---- workspace arrival ---------------------------------------------------
-// Make this thread's earlier global writes visible, then count one arrival
-// for sequence b.  Returns true for exactly one caller: the last of `total`.
+// Count one arrival for sequence b with acquire-release semantics: this
+// thread's earlier writes (and atomics) are visible to whoever arrives later,
+// and the last of `total` arrivals -- the one call that returns true -- sees
+// everything the earlier arrivals wrote.
 __device__ __forceinline__ bool arrive_last(SeqState* seq, int b, unsigned int total) {
-  __threadfence();
-  unsigned int prev = atomicAdd(&seq[b].arrivals, 1u);
-  if (prev + 1u == total) {
-    __threadfence();
-    return true;
-  }
-  return false;
+  return atom_add_acq_rel_gpu(&seq[b].arrivals, 1u) + 1u == total;
 }
 
 #endif  // __CUDACC__

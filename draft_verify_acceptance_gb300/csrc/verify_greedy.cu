@@ -103,38 +103,60 @@ greedy_kernel(VerifyArgs a, long long nvec, int S) {
     s_i[warp] = bidx;
   }
   const int any_bad = __syncthreads_or(bad);
-  if (tid != 0) return;
+  if (warp != 0) return;
 
-  for (int w = 1; w < kWarps; ++w) argmax_merge(best, bidx, s_v[w], s_i[w]);
-  if (any_bad && a.status) atomicOr(a.status, kDataNonfiniteLogit);
+  // warp 0: the block's argmax into the row's key; the last CTA of the
+  // sequence finalises it with the whole warp (all loads at once)
+  unsigned int last = 0;
+  if (lane == 0) {
+    for (int w = 1; w < kWarps; ++w) argmax_merge(best, bidx, s_v[w], s_i[w]);
+    if (any_bad && a.status) atomicOr(a.status, kDataNonfiniteLogit);
+    RowSlot* slots = static_cast<RowSlot*>(a.slots);
+    const unsigned long long key = pack_key(best, bidx);
+    if (S == 1) slots[row].value = key;
+    else atomicMax(&slots[row].value, key);
+    last = arrive_last(a.seq, b, static_cast<unsigned int>(K1) * static_cast<unsigned int>(S)) ? 1u : 0u;
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();  // every lane reads what the other CTAs published
 
-  RowSlot* slots = static_cast<RowSlot*>(a.slots);
-  const unsigned long long key = pack_key(best, bidx);
-  if (S == 1) slots[row].value = key;
-  else atomicMax(&slots[row].value, key);
-
-  if (!arrive_last(a.seq, b, static_cast<unsigned int>(K1) * static_cast<unsigned int>(S)))
-    return;
-
-  // last arrival for sequence b: longest matching prefix, outputs, reset
-  volatile RowSlot* vslots = slots + static_cast<size_t>(b) * K1;
+  // last arrival for sequence b: longest matching prefix, outputs, reset.
+  // Lane l holds positions l, 32 + l, 64 + l (K + 1 <= 65): all loads first.
+  volatile RowSlot* vslots = static_cast<RowSlot*>(a.slots) + static_cast<size_t>(b) * K1;
   const int32_t* x = a.tokens + static_cast<size_t>(b) * a.K;
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
-  int n = a.K;
+  constexpr int kR = (64 + 1 + 31) / 32;
+  int gk[kR], xt[kR];
   bool bad_tok = false;
-  for (int i = 0; i < a.K; ++i) {
-    const int xi = x[i];
-    bad_tok |= (xi < 0 || xi >= a.V);
-    if (n == a.K && xi != key_index(vslots[i].value)) n = i;
+#pragma unroll
+  for (int r = 0; r < kR; ++r) {
+    const int i = r * 32 + lane;
+    gk[r] = (i < K1) ? key_index(vslots[i].value) : 0;
+    xt[r] = (i < a.K) ? x[i] : 0;
+    bad_tok |= (i < a.K) && (xt[r] < 0 || xt[r] >= a.V);
   }
-  for (int i = 0; i < n; ++i) out[i] = x[i];
-  out[n] = key_index(vslots[n].value);
-  for (int i = n + 1; i < K1; ++i) out[i] = -1;
-  a.accepted_len[b] = n;
-  if (a.flags) a.flags[b] = 0;
-  if (bad_tok && a.status) atomicOr(a.status, kDataTokenRange);
-  for (int i = 0; i < K1; ++i) vslots[i].value = 0ull;
-  a.seq[b].arrivals = 0u;
+  int n = a.K;
+#pragma unroll
+  for (int r = 0; r < kR; ++r) {  // the first position whose draft token differs
+    const int i = r * 32 + lane;
+    const unsigned int mism = __ballot_sync(0xffffffffu, i < a.K && xt[r] != gk[r]);
+    if (n == a.K && mism) n = r * 32 + __ffs(mism) - 1;
+  }
+#pragma unroll
+  for (int r = 0; r < kR; ++r) {
+    const int i = r * 32 + lane;
+    if (i < K1) {
+      out[i] = (i < n) ? xt[r] : (i == n ? gk[r] : -1);
+      vslots[i].value = 0ull;
+    }
+  }
+  bad_tok = __any_sync(0xffffffffu, bad_tok);
+  if (lane == 0) {
+    a.accepted_len[b] = n;
+    if (a.flags) a.flags[b] = 0;
+    if (bad_tok && a.status) atomicOr(a.status, kDataTokenRange);
+    a.seq[b].arrivals = 0u;
+  }
 }
 
 template <typename E, int VEC, int U>
