@@ -158,25 +158,56 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+# The sources each kernel is built from (a committed ncu figure stays valid
+# while these hash the same).
+KERNEL_SOURCES = {
+    "greedy_kernel": ["verify_greedy.cu", "device_common.cuh", "launch.h"],
+    "fused_sample_kernel": ["verify_sample_fused.cu", "sample_common.cuh", "device_common.cuh",
+                            "launch.h"],
+    "norm_stream_kernel": ["verify_sample_2p.cu", "sample_common.cuh", "device_common.cuh",
+                           "launch.h"],
+    "sample_kernel": ["verify_sample.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "draft_verify_acceptance_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, only if it was
-    taken on the current kernel sources."""
+def kernel_plan(inp):
+    """(dominant kernel, kernel launches per verify call) for these inputs: the
+    library's dispatch (src: launch_greedy / launch_sample) restated --
+    greedy: one greedy_kernel; sampling with 16-byte aligned rows of at most
+    4096 vectors: one fused_sample_kernel; longer aligned rows (up to the
+    two-kernel sampler's limit): norm_stream_kernel then
+    decide_sample_kernel; otherwise the streaming sample_kernel."""
+    from draft_verify_acceptance_gb300 import workloads as W
+    if inp.mode == W.MODE_GREEDY:
+        return "greedy_kernel", 1
+    esz = 2 if inp.dtype_name == "bf16" else 4
+    if (inp.V * esz) % 16 != 0:
+        return "sample_kernel", 1
+    nvec = inp.V * esz // 16
+    if nvec <= 4096:
+        return "fused_sample_kernel", 1
+    return "norm_stream_kernel", 2
+
+
+def committed_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, only
+    if it was taken on that kernel's current sources."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("kernel") != kernel or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -313,13 +344,13 @@ def run_native(args, rank, world, local):
                    "timing": "CUDA graphs of <=1000 launches, CUDA events on the launch stream"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": committed_traffic(args.workload),
+                     "traffic": committed_traffic(args.workload, kernel_plan(inp)[0]),
                      "algorithmic_bytes_per_launch": nbytes,
-                     "kernel": "greedy_kernel" if inp.mode == W.MODE_GREEDY else "sample_kernel"},
+                     "kernel": kernel_plan(inp)[0]},
         "e2e": {"value": positions * world * e2e_steps / e2e_sec, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "binding.verify on pinned host tensors (H2D, kernel, D2H, sync)"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * kernel_plan(inp)[1],
         "clocks": clk,
         "cpu_baseline": cpu,
         "workloads": extras,
