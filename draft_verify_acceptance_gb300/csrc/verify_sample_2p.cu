@@ -69,7 +69,6 @@ namespace {
 
 constexpr int kStages2 = 4;
 constexpr int kChunk2 = 512;              // vectors per row per stage (8 KiB)
-constexpr int kProducer2 = kThreads - 32;  // issues kernel B's bulk copies
 constexpr int kMaxPending2 = 32;
 
 // Walks [pos, hi) in chunks of at most kChunk2 vectors that never cross a
@@ -297,8 +296,7 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
 }
 
 constexpr int kMaxCB = 8;                // largest cluster of kernel B
-constexpr int kSmemB3 = 72 * 1024;       // slice bytes for three CTAs per SM
-constexpr int kSmemBMax = 200 * 1024;    // slice bytes for one CTA per SM
+constexpr int kSliceB = 2048;            // vectors per row that one CTA of kernel B aims for
 
 // Decision of one sequence, pushed from rank 0 to every CTA of its cluster.
 struct Decision {
@@ -310,8 +308,8 @@ struct Decision {
 };
 
 template <typename E>
-__global__ void __launch_bounds__(kThreads)
-decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
+__global__ void __launch_bounds__(kThreads, 4)
+decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   constexpr int VEC = Staged<E>::kVec;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
@@ -322,11 +320,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
   const float s = a.scale;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  extern __shared__ __align__(128) uint4 smem[];
-  uint4* st = smem;
-  uint4* sd = smem + nvs;
-  unsigned long long* tws = reinterpret_cast<unsigned long long*>(smem + 2 * static_cast<size_t>(nvs));
-  __shared__ __align__(8) unsigned long long bar;
+  extern __shared__ __align__(16) unsigned long long tws[];  // [tiles][warps] slice masses
   __shared__ Decision s_dec;                           // this CTA's decision
   __shared__ unsigned long long s_mass[2][kMaxCB];     // pushed by each rank
   __shared__ int s_tok[2];                             // pushed by the crossing CTA to rank 0
@@ -334,10 +328,6 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
   cluster_arrive_relaxed();  // matched by cluster_wait() before the first DSMEM push
   // everything below reads what the normaliser stream wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    fence_barrier_init();
-  }
 
   // ---- decision (warp 0 of every CTA; identical in all of them) ----------
   // One lane per position: all loads first, then the merge in contributor
@@ -428,49 +418,62 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
   }
   __syncthreads();
 
-  // ---- stage this CTA's slice of row pair n (or of the bonus row) --------
+  // ---- this CTA's slice of row pair n (or of the bonus row) -------------
+  // read straight from global memory (the rows were streamed moments ago;
+  // no staging, so four CTAs fit on an SM and the grid is one wave)
   const Decision dec = s_dec;
   const int n = dec.n;
   bool residual = n < K;
   const long long v0 = nvec * rank / C;
   const int nv = static_cast<int>(nvec * (rank + 1) / C - v0);
   const int ntl = (nv + kThreads - 1) / kThreads;
-  if (tid == kProducer2) {
-    const uint32_t bytes = static_cast<uint32_t>(nv) * 16u;
-    const uint4* trow = static_cast<const uint4*>(a.target) + (static_cast<size_t>(b) * K1 + n) * nvec + v0;
-    mbar_arrive_expect_tx(&bar, residual ? 2u * bytes : bytes);
-    bulk_load(st, trow, bytes, &bar);
-    if (residual)
-      bulk_load(sd, static_cast<const uint4*>(a.draft) + (static_cast<size_t>(b) * K + n) * nvec + v0,
-                bytes, &bar);
-  }
-  if (tid == 0 && !mbar_wait_one(&bar, 0) && !mbar_wait_one(&bar, 0) && a.status)
-    atomicOr(a.status, kWaitTimeout);
-  __syncthreads();
+  const uint4* trow = static_cast<const uint4*>(a.target) + (static_cast<size_t>(b) * K1 + n) * nvec + v0;
+  const uint4* drow = residual
+      ? static_cast<const uint4*>(a.draft) + (static_cast<size_t>(b) * K + n) * nvec + v0
+      : nullptr;
 
-  cluster_wait();  // every CTA of the cluster has started
-  // ---- pass 2: fixed-point mass of the staged slice ----------------------
+  // ---- pass 2: fixed-point mass of the slice, per (tile, warp) ------------
   const float MSt = dec.MSt, MSd = dec.MSd;
   const float invZt = 1.f / dec.Zt;
   const float invZd = residual ? 1.f / dec.Zd : 0.f;
   int rnd = 0;
   unsigned long long S = 0;
   for (;; ++rnd) {
-    for (int k = 0; k < ntl; ++k) {
-      const int v = k * kThreads + tid;
-      float xt[VEC], xd[VEC], r[VEC];
-      if (v < nv) {
-        Staged<E>::unpack(st[v], xt);
-        if (residual) Staged<E>::unpack(sd[v], xd);
-      } else {
+    for (int k0 = 0; k0 < ntl; k0 += 4) {  // four tiles of loads in flight
+      uint4 wt[4], wd[4];
 #pragma unroll
-        for (int q = 0; q < VEC; ++q) xt[q] = xd[q] = -INFINITY;
+      for (int j = 0; j < 4; ++j) {
+        const int v = (k0 + j) * kThreads + tid;
+        if (k0 + j < ntl && v < nv) {
+          wt[j] = ld_stream_v4(trow + v);
+          if (residual) wd[j] = ld_stream_v4(drow + v);
+        }
       }
-      const unsigned long long w =
-          warp_sum_u64(vec_weight_scaled<VEC>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r));
-      if (lane == 0) tws[k * kWarps + warp] = w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int k = k0 + j;
+        if (k < ntl) {  // block-uniform
+          const int v = k * kThreads + tid;
+          float xt[VEC], xd[VEC], r[VEC];
+          if (v < nv) {
+            Staged<E>::unpack(wt[j], xt);
+            if (residual) Staged<E>::unpack(wd[j], xd);
+            else {
+#pragma unroll
+              for (int q = 0; q < VEC; ++q) xd[q] = -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) xt[q] = xd[q] = -INFINITY;
+          }
+          const unsigned long long w = warp_sum_mass(
+              vec_weight_scaled<VEC>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r));
+          if (lane == 0) tws[k * kWarps + warp] = w;
+        }
+      }
     }
     __syncthreads();
+    if (rnd == 0) cluster_wait();  // every CTA of the cluster has started
     if (warp == 0) {
       unsigned long long t = 0;
       for (int k = lane; k < ntl * kWarps; k += 32) t += tws[k];
@@ -485,7 +488,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
   }
 
   // every CTA of the cluster has read the partials and gathers (they were
-  // read before the slice was staged): rank 0 puts its sequence's slots back
+  // read before the first cluster barrier): rank 0 puts its sequence's slots back
   // to zero, keeping the workspace zero-filled between calls
   if (rank == 0 && warp == 0) {
     Partial* partials = static_cast<Partial*>(a.partials);
@@ -545,8 +548,12 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
       const int v = kstar * kThreads + wstar * 32 + lane;
       float xt[VEC], xd[VEC], r[VEC];
       if (v < nv) {
-        Staged<E>::unpack(st[v], xt);
-        if (residual) Staged<E>::unpack(sd[v], xd);
+        Staged<E>::unpack(ld_stream_v4(trow + v), xt);
+        if (residual) Staged<E>::unpack(ld_stream_v4(drow + v), xd);
+        else {
+#pragma unroll
+          for (int q = 0; q < VEC; ++q) xd[q] = -INFINITY;
+        }
       } else {
 #pragma unroll
         for (int q = 0; q < VEC; ++q) xt[q] = xd[q] = -INFINITY;
@@ -603,20 +610,20 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt, int nvs) {
 size_t smem_b(long long nvec, int C) {
   const long long nvs = (nvec + C - 1) / C;
   const long long ntiles = (nvs + kThreads - 1) / kThreads;
-  return static_cast<size_t>(2 * nvs * 16 + ntiles * kWarps * 8);
+  return static_cast<size_t>(ntiles * kWarps * 8);
 }
 
 constexpr int kSmemA = kStages2 * 2 * kChunk2 * 16;
 
 }  // namespace
 
-// Cluster size of kernel B: the smallest C in {1, 2, 4, 8} whose slices fit
-// three CTAs per SM, else 8 if they fit one CTA per SM, else 0 (the rows are
-// too long for this path).
+// Cluster size of kernel B: the smallest C in {1, 2, 4, 8} whose slices are
+// at most kSliceB vectors per row, else 8; 0 when the slice masses would not
+// fit the default shared memory of a CTA.
 int sample_2p_cluster(long long nvec) {
-  for (int C = 1; C <= kMaxCB; C *= 2)
-    if (smem_b(nvec, C) <= static_cast<size_t>(kSmemB3)) return C;
-  return smem_b(nvec, kMaxCB) <= static_cast<size_t>(kSmemBMax) ? kMaxCB : 0;
+  int C = 1;
+  while (C < kMaxCB && (nvec + C - 1) / C > kSliceB) C *= 2;
+  return smem_b(nvec, C) <= 48 * 1024 ? C : 0;
 }
 
 cudaError_t sample_2p_prepare(int* stream_ctas_per_sm) {
@@ -625,12 +632,6 @@ cudaError_t sample_2p_prepare(int* stream_ctas_per_sm) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(norm_stream_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemA);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decide_sample_kernel<BF16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBMax);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decide_sample_kernel<F32>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBMax);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(stream_ctas_per_sm, norm_stream_kernel<BF16>,
                                                       kThreadsA, kSmemA);
@@ -668,7 +669,6 @@ cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
   }
   const long long grid = static_cast<long long>(a.B) * C;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  const int nvs = static_cast<int>((pt.nvec + C - 1) / C);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned int>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -683,8 +683,8 @@ cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16>, a, pt, nvs)
-                : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32>, a, pt, nvs);
+  return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16>, a, pt)
+                : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32>, a, pt);
 }
 
 }  // namespace specv
