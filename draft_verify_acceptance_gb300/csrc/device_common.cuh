@@ -33,7 +33,7 @@ struct __align__(32) SeqState {
   unsigned int pad0;
   unsigned long long reject_mask; // bit i: draft position i was rejected
   unsigned long long near_mask;   // bit i: accept test i was within 1e-6
-  unsigned long long pad1;
+  unsigned long long row_word;    // greedy, one CTA per row: rows done << 48 | mismatch bits
 };
 static_assert(sizeof(SeqState) == 32, "SeqState layout");
 
@@ -331,6 +331,16 @@ __device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* p, un
 // thread's earlier writes (and atomics) are visible to whoever arrives later,
 // and the last of `total` arrivals -- the one call that returns true -- sees
 // everything the earlier arrivals wrote.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long* p,
+                                                                   unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ bool arrive_last(SeqState* seq, int b, unsigned int total) {
   return atom_add_acq_rel_gpu(&seq[b].arrivals, 1u) + 1u == total;
 }

@@ -193,35 +193,76 @@ struct RowAcc {
   float ms, z;
 };
 
+// Packed fp32 pair arithmetic (two lanes per instruction, each rounded as the
+// scalar operation would be).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
+      "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// The VEC elements of a 16-byte vector as VEC/2 fp32 pairs, in element order.
+template <typename E>
+__device__ __forceinline__ void unpack_pairs(const uint4 w, float2 (&x)[Staged<E>::kVec / 2]) {
+  if constexpr (Staged<E>::kVec == 8) {
+    x[0] = make_float2(bf16_lo(w.x), bf16_hi(w.x));
+    x[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+    x[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
+    x[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
+  } else {
+    x[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+    x[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+  }
+}
+
 // Fold up to two 16-byte vectors held in registers into a row accumulator
 // without branches (so independent rows of a stage interleave): the new
 // offset is the larger of the old one and the vectors' packed maximum, the
 // old sum is rescaled by 2^(old - new) (exactly 1 when unchanged), and each
-// logit adds 2^(x*s - new) with one FFMA + ex2, summed as a tree.  An
+// logit adds 2^(x*s - new), summed as a tree.  The FFMAs and the tree's adds
+// run on fp32 pairs (same roundings, same order as the scalar form).  An
 // accumulator that has seen no finite logit stays at (-inf, 0).  kFull: both
 // vectors are valid (nvalid == 2), so there are no per-element selects.
 template <typename E, bool kFull>
 __device__ __forceinline__ void acc_vectors_impl(RowAcc& A, const uint4 (&w)[2], int nvalid, float s) {
   constexpr int VEC = Staged<E>::kVec;
+  constexpr int NP = VEC;  // pairs in two vectors
   typename Staged<E>::Max pm = Staged<E>::max_init();
   if (kFull || nvalid > 0) Staged<E>::max_update(pm, w[0]);
   if (kFull || nvalid > 1) Staged<E>::max_update(pm, w[1]);
   const float nm = fmaxf(A.ms, Staged<E>::max_value(pm) * s);
   const float f = (A.ms == nm) ? 1.f : ex2(A.ms - nm);
-  float e[2 * VEC];
+  const float2 s2 = make_float2(s, s), nm2 = make_float2(-nm, -nm);
+  float2 e[NP];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    float x[VEC];
-    Staged<E>::unpack(w[j], x);
+    float2 x[VEC / 2];
+    unpack_pairs<E>(w[j], x);
 #pragma unroll
-    for (int k = 0; k < VEC; ++k)
-      e[j * VEC + k] = (kFull || j < nvalid) ? ex2(fmaf(x[k], s, -nm)) : 0.f;
+    for (int k = 0; k < VEC / 2; ++k) {
+      const float2 t = ffma2(x[k], s2, nm2);
+      e[j * (VEC / 2) + k] = (kFull || j < nvalid) ? make_float2(ex2(t.x), ex2(t.y))
+                                                   : make_float2(0.f, 0.f);
+    }
   }
 #pragma unroll
-  for (int h = VEC; h > 0; h >>= 1)
+  for (int h = NP / 2; h > 0; h >>= 1)
 #pragma unroll
-    for (int k = 0; k < h; ++k) e[k] += e[k + h];
-  const float zn = fmaf(A.z, f, e[0]);
+    for (int k = 0; k < h; ++k) e[k] = fadd2(e[k], e[k + h]);
+  const float zn = fmaf(A.z, f, e[0].x + e[0].y);
   A.z = (nm == -INFINITY) ? 0.f : zn;
   A.ms = nm;
 }

@@ -6,12 +6,21 @@
 // token g_n is emitted at the first mismatch n (or at K when all match).
 //
 // Design: the [B*(K+1), V] logit rows are streamed once from HBM with 16-byte
-// non-allocating loads.  Each row is split into S segments, one CTA each, so
-// that the whole grid is resident in about one wave; a CTA reduces its
-// segment to (max value, lowest index) and folds it into the row's packed
-// 64-bit key with one atomicMax.  The CTA that arrives last for a sequence
-// (a counter in the workspace, no waiting) compares the K+1 argmaxes with
-// the draft tokens, writes the outputs and puts the workspace back to zero.
+// non-allocating loads, the next batch in flight while the current one is
+// reduced.  Each row is split into S segments, one CTA each, so that the
+// whole grid is resident in about one wave.  A thread keeps the first 16-byte
+// vector holding its largest value (one NaN-propagating packed max per
+// vector, no per-element index bookkeeping) and finds the element inside it
+// at the end; the CTA reduces to (max value, lowest index).
+//   One CTA per row (S == 1, K + 1 <= 48): the CTA writes g_i to its output
+//   slot and adds (1 << 48 | mismatch bit i) to its sequence's word with one
+//   acquire-release atomic; the CTA that completes the count knows n from the
+//   mismatch bits and only overwrites the padding and writes n.
+//   Several CTAs per row: each folds its result into the row's packed 64-bit
+//   key with one atomicMax and counts itself on the sequence; the last CTA
+//   loads the K+1 keys, compares them with the draft tokens and writes the
+//   outputs.
+// Either way no CTA waits, and the workspace is put back to zero.
 #include <cfloat>
 #include <climits>
 
@@ -45,44 +54,139 @@ __device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2)
   }
 }
 
+// NaN-propagating maximum of a 16-byte vector, as fp32 (NaN if it holds a NaN).
+template <typename E>
+struct VecMax;
+template <>
+struct VecMax<BF16> {
+  static constexpr uint32_t kNegInf = 0xff80ff80u;
+  static __device__ __forceinline__ uint32_t mx(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  static __device__ __forceinline__ float of(const uint4 w) {
+    uint32_t m = mx(mx(w.x, w.y), mx(w.z, w.w));
+    m = mx(m, __byte_perm(m, 0u, 0x1032));  // both halves: the vector's maximum
+    return bf16_hi(m);
+  }
+  static __device__ __forceinline__ void unpack(const uint4 w, float (&x)[8]) {
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+  }
+};
+template <>
+struct VecMax<F32> {
+  static constexpr uint32_t kNegInf = 0xff800000u;
+  static __device__ __forceinline__ float mx(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+  }
+  static __device__ __forceinline__ float of(const uint4 w) {
+    return mx(mx(__uint_as_float(w.x), __uint_as_float(w.y)),
+              mx(__uint_as_float(w.z), __uint_as_float(w.w)));
+  }
+  static __device__ __forceinline__ void unpack(const uint4 w, float (&x)[4]) {
+    x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+  }
+};
+
+// Largest value of this thread's vectors v0 + tid + j*kThreads (< v1) and the
+// lowest index holding it; a vector with a NaN is skipped (and flagged).
+template <typename E, int VEC, int U>
+__device__ __forceinline__ void thread_argmax_vec(const uint4* row, long long v0, long long v1,
+                                                 float& best, int& bidx, bool& bad) {
+  constexpr uint32_t ni = VecMax<E>::kNegInf;
+  constexpr long long kStep = static_cast<long long>(kThreads) * U;
+  const int tid = threadIdx.x;
+  long long bv = -1;
+  uint4 bw = make_uint4(ni, ni, ni, ni);
+  uint4 cur[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long vv = v0 + tid + static_cast<long long>(u) * kThreads;
+    cur[u] = vv < v1 ? ld_stream_v4(row + vv) : make_uint4(ni, ni, ni, ni);
+  }
+  for (long long v = v0 + tid; v < v1; v += kStep) {
+    uint4 nxt[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {  // the next batch is in flight while this one is reduced
+      const long long vv = v + kStep + static_cast<long long>(u) * kThreads;
+      nxt[u] = vv < v1 ? ld_stream_v4(row + vv) : make_uint4(ni, ni, ni, ni);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float f = VecMax<E>::of(cur[u]);
+      bad |= !(f <= FLT_MAX);  // NaN or +inf
+      if (f > best) {
+        best = f;
+        bv = v + static_cast<long long>(u) * kThreads;
+        bw = cur[u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+  }
+  if (bv >= 0) {
+    float x[VEC];
+    VecMax<E>::unpack(bw, x);
+    int k = VEC - 1;
+#pragma unroll
+    for (int j = VEC - 1; j >= 0; --j)
+      if (x[j] == best) k = j;
+    bidx = static_cast<int>(bv * VEC + k);
+  }
+}
+
 template <typename E, int VEC, int U>
 __global__ void __launch_bounds__(kThreads)
-greedy_kernel(VerifyArgs a, long long nvec, int S) {
+greedy_kernel(VerifyArgs a, long long nvec, int S, bool one_word) {
   const int K1 = a.K + 1;
   const long long row = blockIdx.x / S;
   const int seg = static_cast<int>(blockIdx.x - row * S);
   const int b = static_cast<int>(row / K1);
+  const int pos = static_cast<int>(row - static_cast<long long>(b) * K1);
   const long long v0 = nvec * seg / S;
   const long long v1 = nvec * (seg + 1) / S;
   const char* base = static_cast<const char*>(a.target) +
                      static_cast<size_t>(row) * static_cast<size_t>(a.V) * E::kBytes;
 
   const int tid = threadIdx.x;
+  // the draft token this row is compared with, fetched while the row streams
+  int xtok = 0;
+  if (one_word && tid == 0 && pos < a.K) xtok = a.tokens[static_cast<size_t>(b) * a.K + pos];
+
   float best = -INFINITY;
   int bidx = (v0 + tid < v1) ? static_cast<int>((v0 + tid) * VEC) : INT_MAX;
   bool bad = false;
 
-  for (long long v = v0 + tid; v < v1; v += static_cast<long long>(kThreads) * U) {
-    float x[U][VEC];
+  if constexpr (VEC > 1) {
+    thread_argmax_vec<E, VEC, U>(reinterpret_cast<const uint4*>(base), v0, v1, best, bidx, bad);
+  } else {
+    for (long long v = v0 + tid; v < v1; v += static_cast<long long>(kThreads) * U) {
+      float x[U][VEC];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long vv = v + static_cast<long long>(u) * kThreads;
-      if (vv < v1) {
-        VecLoad<E, VEC>::load(base, vv, x[u]);
-      } else {
+      for (int u = 0; u < U; ++u) {
+        const long long vv = v + static_cast<long long>(u) * kThreads;
+        if (vv < v1) {
+          VecLoad<E, VEC>::load(base, vv, x[u]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) x[u][k] = -INFINITY;
+          for (int k = 0; k < VEC; ++k) x[u][k] = -INFINITY;
+        }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+      for (int u = 0; u < U; ++u) {
 #pragma unroll
-      for (int k = 0; k < VEC; ++k) {
-        const float e = x[u][k];
-        bad |= !(e <= FLT_MAX);  // NaN or +inf
-        if (e > best) {
-          best = e;
-          bidx = static_cast<int>((v + static_cast<long long>(u) * kThreads) * VEC + k);
+        for (int k = 0; k < VEC; ++k) {
+          const float e = x[u][k];
+          bad |= !(e <= FLT_MAX);  // NaN or +inf
+          if (e > best) {
+            best = e;
+            bidx = static_cast<int>((v + static_cast<long long>(u) * kThreads) * VEC + k);
+          }
         }
       }
     }
@@ -104,6 +208,31 @@ greedy_kernel(VerifyArgs a, long long nvec, int S) {
   }
   const int any_bad = __syncthreads_or(bad);
   if (warp != 0) return;
+
+  if (one_word) {  // one CTA per row: g_i to its slot, one atomic on the sequence
+    if (lane == 0) {
+      for (int w = 1; w < kWarps; ++w) argmax_merge(best, bidx, s_v[w], s_i[w]);
+      int flags = any_bad ? kDataNonfiniteLogit : 0;
+      bool mism = true;  // the bonus position always ends the prefix
+      if (pos < a.K) {
+        mism = xtok != bidx;
+        if (xtok < 0 || xtok >= a.V) flags |= kDataTokenRange;
+      }
+      if (flags && a.status) atomicOr(a.status, flags);
+      int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
+      out[pos] = bidx;  // x_i when it matches, g_n at the first mismatch
+      const unsigned long long add = (1ull << 48) | (mism ? (1ull << pos) : 0ull);
+      const unsigned long long now = atom_add_acq_rel_gpu(&a.seq[b].row_word, add) + add;
+      if (static_cast<int>(now >> 48) == K1) {  // every row of the sequence is done
+        const int n = __ffsll(static_cast<long long>(now & ((1ull << 48) - 1))) - 1;
+        for (int i = n + 1; i < K1; ++i) out[i] = -1;
+        a.accepted_len[b] = n;
+        if (a.flags) a.flags[b] = 0;
+        a.seq[b].row_word = 0ull;
+      }
+    }
+    return;
+  }
 
   // warp 0: the block's argmax into the row's key; the last CTA of the
   // sequence finalises it with the whole warp (all loads at once)
@@ -159,6 +288,10 @@ greedy_kernel(VerifyArgs a, long long nvec, int S) {
   }
 }
 
+// Sequences of at most this many rows keep their mismatch bits and row count
+// in one 64-bit word (count in the top 16 bits).
+constexpr int kOneWordRows = 48;
+
 template <typename E, int VEC, int U>
 cudaError_t launch_greedy_t(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   const long long nvec = a.V / VEC;
@@ -171,7 +304,8 @@ cudaError_t launch_greedy_t(const VerifyArgs& a, const DeviceInfo& dev, cudaStre
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, greedy_kernel<E, VEC, U>, a, nvec, S);
+  const bool one_word = S == 1 && a.K + 1 <= kOneWordRows;
+  return cudaLaunchKernelEx(&cfg, greedy_kernel<E, VEC, U>, a, nvec, S, one_word);
 }
 
 }  // namespace
