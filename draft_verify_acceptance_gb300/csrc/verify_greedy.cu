@@ -95,39 +95,36 @@ struct VecMax<F32> {
 
 // Largest value of this thread's vectors v0 + tid + j*kThreads (< v1) and the
 // lowest index holding it; a vector with a NaN is skipped (and flagged).
+// Vector indices within a row fit in int (V <= 2^22).
 template <typename E, int VEC, int U>
-__device__ __forceinline__ void thread_argmax_vec(const uint4* row, long long v0, long long v1,
+__device__ __forceinline__ void thread_argmax_vec(const uint4* row, int v0, int v1,
                                                  float& best, int& bidx, bool& bad) {
   constexpr uint32_t ni = VecMax<E>::kNegInf;
-  constexpr long long kStep = static_cast<long long>(kThreads) * U;
+  constexpr int kStep = kThreads * U;
   const int tid = threadIdx.x;
-  long long bv = -1;
+  int bv = -1;
   uint4 bw = make_uint4(ni, ni, ni, ni);
   uint4 cur[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const long long vv = v0 + tid + static_cast<long long>(u) * kThreads;
+    const int vv = v0 + tid + u * kThreads;
     cur[u] = vv < v1 ? ld_stream_v4(row + vv) : make_uint4(ni, ni, ni, ni);
   }
-  for (long long v = v0 + tid; v < v1; v += kStep) {
-    uint4 nxt[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {  // the next batch is in flight while this one is reduced
-      const long long vv = v + kStep + static_cast<long long>(u) * kThreads;
-      nxt[u] = vv < v1 ? ld_stream_v4(row + vv) : make_uint4(ni, ni, ni, ni);
-    }
+  for (int v = v0 + tid; v < v1; v += kStep) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      // reduce vector u of this batch, then put the next batch's vector u in
+      // flight in its place (the loads of a batch overlap the reduction)
       const float f = VecMax<E>::of(cur[u]);
       bad |= !(f <= FLT_MAX);  // NaN or +inf
       if (f > best) {
         best = f;
-        bv = v + static_cast<long long>(u) * kThreads;
+        bv = v + u * kThreads;
         bw = cur[u];
       }
+      const int vv = v + kStep + u * kThreads;
+      cur[u] = vv < v1 ? ld_stream_v4(row + vv) : make_uint4(ni, ni, ni, ni);
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) cur[u] = nxt[u];
   }
   if (bv >= 0) {
     float x[VEC];
@@ -136,12 +133,12 @@ __device__ __forceinline__ void thread_argmax_vec(const uint4* row, long long v0
 #pragma unroll
     for (int j = VEC - 1; j >= 0; --j)
       if (x[j] == best) k = j;
-    bidx = static_cast<int>(bv * VEC + k);
+    bidx = bv * VEC + k;
   }
 }
 
 template <typename E, int VEC, int U>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: four CTAs per SM
 greedy_kernel(VerifyArgs a, long long nvec, int S, bool one_word) {
   const int K1 = a.K + 1;
   const long long row = blockIdx.x / S;
@@ -163,7 +160,8 @@ greedy_kernel(VerifyArgs a, long long nvec, int S, bool one_word) {
   bool bad = false;
 
   if constexpr (VEC > 1) {
-    thread_argmax_vec<E, VEC, U>(reinterpret_cast<const uint4*>(base), v0, v1, best, bidx, bad);
+    thread_argmax_vec<E, VEC, U>(reinterpret_cast<const uint4*>(base), static_cast<int>(v0),
+                                 static_cast<int>(v1), best, bidx, bad);
   } else {
     for (long long v = v0 + tid; v < v1; v += static_cast<long long>(kThreads) * U) {
       float x[U][VEC];
@@ -326,15 +324,15 @@ int greedy_segments(long long rows, long long nvec, int sm_count, int ctas_per_s
 
 cudaError_t greedy_occupancy(int* ctas_per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm,
-                                                       greedy_kernel<BF16, 8, 4>, kThreads, 0);
+                                                       greedy_kernel<BF16, 8, 8>, kThreads, 0);
 }
 
 cudaError_t launch_greedy(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   if (a.bf16) {
-    return a.vec ? launch_greedy_t<BF16, 8, 4>(a, dev, stream)
+    return a.vec ? launch_greedy_t<BF16, 8, 8>(a, dev, stream)
                  : launch_greedy_t<BF16, 1, 8>(a, dev, stream);
   }
-  return a.vec ? launch_greedy_t<F32, 4, 4>(a, dev, stream)
+  return a.vec ? launch_greedy_t<F32, 4, 8>(a, dev, stream)
                : launch_greedy_t<F32, 1, 8>(a, dev, stream);
 }
 
