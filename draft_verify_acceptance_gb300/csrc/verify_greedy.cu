@@ -47,13 +47,6 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
   return static_cast<int>(0xffffffffu - static_cast<unsigned int>(key & 0xffffffffull));
 }
 
-__device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2) {
-  if (v2 > v || (v2 == v && i2 < i)) {
-    v = v2;
-    i = i2;
-  }
-}
-
 // NaN-propagating maximum of a 16-byte vector, as fp32 (NaN if it holds a NaN).
 template <typename E>
 struct VecMax;
@@ -139,35 +132,36 @@ __device__ __forceinline__ void thread_argmax_vec(const uint4* row, int v0, int 
 
 template <typename E, int VEC, int U>
 __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: four CTAs per SM
-greedy_kernel(VerifyArgs a, long long nvec, int S, bool one_word) {
+greedy_kernel(VerifyArgs a, int nvec, int S, bool one_word) {
+  // 32-bit index arithmetic: the grid fits int and nvec * S <= 2^22 * 64
   const int K1 = a.K + 1;
-  const long long row = blockIdx.x / S;
-  const int seg = static_cast<int>(blockIdx.x - row * S);
-  const int b = static_cast<int>(row / K1);
-  const int pos = static_cast<int>(row - static_cast<long long>(b) * K1);
-  const long long v0 = nvec * seg / S;
-  const long long v1 = nvec * (seg + 1) / S;
+  const int row = static_cast<int>(blockIdx.x) / S;
+  const int seg = static_cast<int>(blockIdx.x) - row * S;
+  const int v0 = nvec * seg / S;
+  const int v1 = nvec * (seg + 1) / S;
   const char* base = static_cast<const char*>(a.target) +
                      static_cast<size_t>(row) * static_cast<size_t>(a.V) * E::kBytes;
 
   const int tid = threadIdx.x;
   // the draft token this row is compared with, fetched while the row streams
   int xtok = 0;
-  if (one_word && tid == 0 && pos < a.K) xtok = a.tokens[static_cast<size_t>(b) * a.K + pos];
+  if (one_word && tid == 0) {
+    const int b = row / K1, pos = row - b * K1;
+    if (pos < a.K) xtok = a.tokens[static_cast<size_t>(b) * a.K + pos];
+  }
 
   float best = -INFINITY;
-  int bidx = (v0 + tid < v1) ? static_cast<int>((v0 + tid) * VEC) : INT_MAX;
+  int bidx = (v0 + tid < v1) ? (v0 + tid) * VEC : INT_MAX;
   bool bad = false;
 
   if constexpr (VEC > 1) {
-    thread_argmax_vec<E, VEC, U>(reinterpret_cast<const uint4*>(base), static_cast<int>(v0),
-                                 static_cast<int>(v1), best, bidx, bad);
+    thread_argmax_vec<E, VEC, U>(reinterpret_cast<const uint4*>(base), v0, v1, best, bidx, bad);
   } else {
-    for (long long v = v0 + tid; v < v1; v += static_cast<long long>(kThreads) * U) {
+    for (int v = v0 + tid; v < v1; v += kThreads * U) {
       float x[U][VEC];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const long long vv = v + static_cast<long long>(u) * kThreads;
+        const int vv = v + u * kThreads;
         if (vv < v1) {
           VecLoad<E, VEC>::load(base, vv, x[u]);
         } else {
@@ -183,33 +177,38 @@ greedy_kernel(VerifyArgs a, long long nvec, int S, bool one_word) {
           bad |= !(e <= FLT_MAX);  // NaN or +inf
           if (e > best) {
             best = e;
-            bidx = static_cast<int>((v + static_cast<long long>(u) * kThreads) * VEC + k);
+            bidx = (v + u * kThreads) * VEC + k;
           }
         }
       }
     }
   }
 
-  // block argmax: warp butterfly, then across warps in a fixed order
+  // block argmax on packed keys (larger value, then lower index, wins):
+  // warp butterfly, then the kWarps warp keys butterflied by warp 0
+  unsigned long long key = pack_key(best, bidx);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, best, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, bidx, off);
-    argmax_merge(best, bidx, ov, oi);
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+    key = o > key ? o : key;
   }
-  __shared__ float s_v[kWarps];
-  __shared__ int s_i[kWarps];
+  __shared__ unsigned long long s_key[kWarps];
   const int warp = tid >> 5, lane = tid & 31;
-  if (lane == 0) {
-    s_v[warp] = best;
-    s_i[warp] = bidx;
-  }
+  if (lane == 0) s_key[warp] = key;
   const int any_bad = __syncthreads_or(bad);
   if (warp != 0) return;
+  key = s_key[lane & (kWarps - 1)];
+#pragma unroll
+  for (int off = kWarps / 2; off > 0; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+    key = o > key ? o : key;
+  }
+  const int b = row / K1;
 
   if (one_word) {  // one CTA per row: g_i to its slot, one atomic on the sequence
     if (lane == 0) {
-      for (int w = 1; w < kWarps; ++w) argmax_merge(best, bidx, s_v[w], s_i[w]);
+      const int pos = row - b * K1;
+      bidx = key_index(key);
       int flags = any_bad ? kDataNonfiniteLogit : 0;
       bool mism = true;  // the bonus position always ends the prefix
       if (pos < a.K) {
@@ -236,10 +235,8 @@ greedy_kernel(VerifyArgs a, long long nvec, int S, bool one_word) {
   // sequence finalises it with the whole warp (all loads at once)
   unsigned int last = 0;
   if (lane == 0) {
-    for (int w = 1; w < kWarps; ++w) argmax_merge(best, bidx, s_v[w], s_i[w]);
     if (any_bad && a.status) atomicOr(a.status, kDataNonfiniteLogit);
     RowSlot* slots = static_cast<RowSlot*>(a.slots);
-    const unsigned long long key = pack_key(best, bidx);
     if (S == 1) slots[row].value = key;
     else atomicMax(&slots[row].value, key);
     last = arrive_last(a.seq, b, static_cast<unsigned int>(K1) * static_cast<unsigned int>(S)) ? 1u : 0u;
@@ -303,7 +300,7 @@ cudaError_t launch_greedy_t(const VerifyArgs& a, const DeviceInfo& dev, cudaStre
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   const bool one_word = S == 1 && a.K + 1 <= kOneWordRows;
-  return cudaLaunchKernelEx(&cfg, greedy_kernel<E, VEC, U>, a, nvec, S, one_word);
+  return cudaLaunchKernelEx(&cfg, greedy_kernel<E, VEC, U>, a, static_cast<int>(nvec), S, one_word);
 }
 
 }  // namespace

@@ -126,6 +126,9 @@ GREEDY_CASES = [
     ("bf16_K0", 8, 0, 2000, torch.bfloat16, dict(target_std=3.0)),
     ("f32_Kmax", 3, 64, 200, torch.float32, dict(target_std=3.0, greedy_noise=0.01)),
     ("f32_V1", 4, 2, 1, torch.float32, dict()),
+    # one CTA per row and K + 1 = 48: the largest sequence whose row count and
+    # mismatch bits share one 64-bit word
+    ("bf16_K47_one_word", 4, 47, 3000, torch.bfloat16, dict(target_std=3.0, greedy_noise=0.01)),
 ]
 
 
