@@ -39,6 +39,9 @@ struct DeviceInfo {
   int sm_count = 0;
   int greedy_ctas_per_sm = 0;  // occupancy of the greedy kernel
   int stream_ctas_per_sm = 0;  // occupancy of the two-kernel sampler's streaming pass
+  // clusters of the two-kernel sampler's second kernel that fit at once:
+  // [256, 512, 1024 threads][cluster size 1, 2, 4, 8]
+  int decide_clusters[3][4] = {};
 };
 
 cudaError_t device_info(int device, DeviceInfo* out);
@@ -60,7 +63,7 @@ cudaError_t launch_sample_fused(const VerifyArgs& a, const DeviceInfo& dev, cuda
 // The two-kernel sampler (normaliser stream, then decide and draw with one
 // cluster per sequence) for rows whose draw spans several draw segments.
 int sample_2p_cluster(long long nvec);
-cudaError_t sample_2p_prepare(int* stream_ctas_per_sm);
+cudaError_t sample_2p_prepare(DeviceInfo* d);
 cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
                              cudaStream_t stream);
 

@@ -8,15 +8,64 @@
 
 namespace specv {
 
-constexpr float kFix = 72057594037927936.0f;  // 2^56: fixed-point scale of probabilities
 constexpr float kBandF = 1e-6f;               // boundary band of the ratio test
+
+// round(2^56 * acc) to nearest, ties to even, for a finite acc in [0, 2^7),
+// with integer operations only: acc = m * 2^(e - 150) (m with its implicit
+// bit), so 2^56 * acc = m * 2^(e - 94).  The same value as fix56_cvt (the
+// hardware conversion of the exact product 2^56 * acc), with a shorter
+// latency: the 64-bit float-to-integer conversion runs on a narrow pipe of
+// this GPU (about 100 cycles, 2 results per clock per SM).  Latency-bound
+// steps (one lane walking a vector's elements) use this form; bulk passes,
+// where the conversions overlap with other work, use fix56_cvt.
+__device__ __forceinline__ unsigned long long fix56(float acc) {
+  const unsigned int u = __float_as_uint(acc);
+  const int e = static_cast<int>(u >> 23);  // acc >= +0: no sign bit
+  const unsigned int m = (u & 0x7fffffu) | 0x800000u;
+  if (e >= 94) return static_cast<unsigned long long>(m) << (e - 94);
+  const int sh = 94 - e;                    // 2^56 * acc < 0.5 when sh >= 25
+  if (sh >= 25) return 0ull;
+  const unsigned int q = m >> sh;
+  const unsigned int rem = m & ((1u << sh) - 1u), half = 1u << (sh - 1);
+  return q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u);
+}
+
+__device__ __forceinline__ unsigned long long fix56_cvt(float acc) {
+  return __float2ull_rn(__fmul_rn(acc, 72057594037927936.0f));  // 2^56 * acc is exact
+}
+
+// The draw's threshold floor(u * S), exactly, for u in [0, 1): u = m * 2^(e -
+// 150), so u * S = (m * S) >> (150 - e) with the 88-bit product m * S formed
+// in two 64-bit halves.  u <= 0 or NaN gives 0, u >= 1 gives S - 1.
+__device__ __forceinline__ unsigned long long draw_threshold(float u, unsigned long long S) {
+  if (!(u > 0.f)) return 0ull;
+  if (!(u < 1.f)) return S - 1;
+  const unsigned int b = __float_as_uint(u);
+  const int e = static_cast<int>(b >> 23);
+  if (e == 0) return 0ull;                  // subnormal u: u * S < 1
+  const unsigned long long m = (b & 0x7fffffu) | 0x800000u;
+  const int sh = 150 - e;                   // >= 24 since u < 1
+  const unsigned long long lo = m * S, hi = __umul64hi(m, S);
+  if (sh >= 64) return sh >= 128 ? 0ull : hi >> (sh - 64);
+  return (lo >> sh) | (hi << (64 - sh));
+}
+
+// Whether the threshold lies within 1e-6 * S of either end [lo, hi) of the
+// chosen element's step of the fixed-point CDF.
+__device__ __forceinline__ bool near_step(unsigned long long theta, unsigned long long lo,
+                                          unsigned long long hi, unsigned long long S) {
+  const unsigned long long band = __umul64hi(S, 18446744073710ull);  // 1e-6 * 2^64
+  const unsigned long long dl = theta >= lo ? theta - lo : lo - theta;
+  const unsigned long long dh = hi >= theta ? hi - theta : theta - hi;
+  return dl < band || dh < band;
+}
 
 // The residual weights r_k = max(0, p_k - q_k) (or p_k when `residual` is
 // false) of one vector and the vector's fixed-point mass round(2^56 * sum r).
 // The fp32 sum runs in element order with explicitly rounded operations, so
 // every recomputation is bit-identical and integer sums of masses agree
-// exactly in any order.
-template <int VEC>
+// exactly in any order.  kInt: round with fix56 (latency-bound callers).
+template <int VEC, bool kInt = false>
 __device__ __forceinline__ unsigned long long vec_weight(const float (&xt)[VEC],
                                                          const float (&xd)[VEC], float Mt,
                                                          float invZt, float Md, float invZd,
@@ -34,14 +83,14 @@ __device__ __forceinline__ unsigned long long vec_weight(const float (&xt)[VEC],
     r[k] = rk;
     acc = __fadd_rn(acc, rk);
   }
-  return __float2ull_rn(__fmul_rn(acc, kFix));
+  return kInt ? fix56(acc) : fix56_cvt(acc);
 }
 
 // The same weights with the normalisers kept relative to scaled offsets
 // MSt = round(Mt * s), MSd = round(Md * s): p_k = 2^fma(x_k, s, -MSt) / Zt.
 // One fused multiply-add per logit; the offset's rounding is common to every
 // term of the row and to its normaliser, so it cancels.
-template <int VEC>
+template <int VEC, bool kInt = false>
 __device__ __forceinline__ unsigned long long vec_weight_scaled(
     const float (&xt)[VEC], const float (&xd)[VEC], float MSt, float invZt, float MSd,
     float invZd, float s, bool residual, float (&r)[VEC]) {
@@ -57,7 +106,7 @@ __device__ __forceinline__ unsigned long long vec_weight_scaled(
     r[k] = rk;
     acc = __fadd_rn(acc, rk);
   }
-  return __float2ull_rn(__fmul_rn(acc, kFix));
+  return kInt ? fix56(acc) : fix56_cvt(acc);
 }
 
 // Merge two normalisers kept relative to scaled offsets (ms, z): the result
@@ -136,7 +185,7 @@ __device__ __forceinline__ int pick_in_vector(const float (&r)[VEC], unsigned lo
 #pragma unroll
   for (int k = 0; k < VEC; ++k) {
     acc = __fadd_rn(acc, r[k]);
-    const unsigned long long cc = __float2ull_rn(__fmul_rn(acc, kFix));
+    const unsigned long long cc = fix56(acc);
     if (cc > rem) {
       mstar = k;
       c_cur = cc;

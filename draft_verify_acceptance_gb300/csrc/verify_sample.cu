@@ -260,10 +260,7 @@ sample_kernel(VerifyArgs a, long long nvec, int ntiles) {
     }
     return;
   }
-  double th = static_cast<double>(uK) * static_cast<double>(S);
-  if (!(th >= 0.0)) th = 0.0;
-  const unsigned long long theta =
-      (th >= static_cast<double>(S)) ? S - 1 : static_cast<unsigned long long>(th);
+  const unsigned long long theta = draw_threshold(uK, S);
   // the slice holding the crossing: first rank whose running total passes theta
   int cstar = C - 1;
   unsigned long long off = 0;
@@ -315,7 +312,7 @@ sample_kernel(VerifyArgs a, long long nvec, int ntiles) {
   float xt[VEC], xd[VEC], r[VEC];
   load_or_pad<E, VEC>(trow, vv, v1, xt);
   if (residual) load_or_pad<E, VEC>(drow, vv, v1, xd);
-  const unsigned long long w = vec_weight<VEC>(xt, xd, Mt, invZt, Md, invZd, s, residual, r);
+  const unsigned long long w = vec_weight<VEC, true>(xt, xd, Mt, invZt, Md, invZd, s, residual, r);
   unsigned long long incl = w;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -333,15 +330,12 @@ sample_kernel(VerifyArgs a, long long nvec, int ntiles) {
 #pragma unroll
   for (int k = 0; k < VEC; ++k) {
     acc = __fadd_rn(acc, r[k]);
-    const unsigned long long c = __float2ull_rn(__fmul_rn(acc, kFix));
+    const unsigned long long c = fix56(acc);
     if (c > rem) { mstar = k; c_cur = c; break; }
     c_prev = c;
   }
   const long long token = vv * VEC + mstar;
-  const double band = 1e-6 * static_cast<double>(S);
-  const double lo = static_cast<double>(off + before + c_prev);
-  const double hi = static_cast<double>(off + before + c_cur);
-  const bool near = fabs(th - lo) < band || fabs(hi - th) < band;
+  const bool near = near_step(theta, off + before + c_prev, off + before + c_cur, S);
   const int32_t tok = static_cast<int32_t>(token < a.V ? token : a.V - 1);
   slots[my_slot] = near ? static_cast<int32_t>(static_cast<uint32_t>(tok) | 0x80000000u) : tok;
   if (arrive_last(a.seq, b, static_cast<unsigned int>(K1))) finalize_sequence(a, b);

@@ -22,12 +22,14 @@
 // plain store.  The CTA that streams the vector holding x_i stores t[x_i] and
 // d[x_i].
 // Kernel B (decide and sample), launched as a programmatic dependent of A:
-// one cluster per sequence.  Warp 0 of rank 0 merges each row's partials in
-// contributor order, runs the K accept tests in parallel lanes and finds the
-// first rejection n with a ballot; every CTA of the cluster then stages its
-// slice of row pair n (or of the bonus row) with one bulk copy and the
-// fixed-point inverse CDF of the staged kernel picks the token.  Rank 0
-// writes the outputs.  Kernel B re-reads about one row pair per sequence.
+// one cluster per sequence.  Warp 0 of every CTA merges each row's partials
+// in contributor order, runs the K accept tests in parallel lanes and finds
+// the first rejection n with a ballot; every CTA of the cluster then reads its
+// slice of row pair n (or of the bonus row) from global memory and computes
+// its fixed-point residual mass, the CTAs exchange slice masses through
+// distributed shared memory, and the CTA holding the crossing finds the
+// token.  Rank 0 writes the outputs.  Kernel B re-reads one row pair per
+// sequence.
 #include <cooperative_groups.h>
 
 #include <cfloat>
@@ -307,9 +309,10 @@ struct Decision {
   int pad;
 };
 
-template <typename E>
-__global__ void __launch_bounds__(kThreads, 4)
+template <typename E, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT)  // <= 64 registers
 decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
+  constexpr int kTB = NT, kWB = NT / 32;  // threads, warps
   constexpr int VEC = Staged<E>::kVec;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
@@ -426,7 +429,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   bool residual = n < K;
   const long long v0 = nvec * rank / C;
   const int nv = static_cast<int>(nvec * (rank + 1) / C - v0);
-  const int ntl = (nv + kThreads - 1) / kThreads;
+  const int ntl = (nv + kTB - 1) / kTB;
   const uint4* trow = static_cast<const uint4*>(a.target) + (static_cast<size_t>(b) * K1 + n) * nvec + v0;
   const uint4* drow = residual
       ? static_cast<const uint4*>(a.draft) + (static_cast<size_t>(b) * K + n) * nvec + v0
@@ -443,7 +446,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
       uint4 wt[4], wd[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int v = (k0 + j) * kThreads + tid;
+        const int v = (k0 + j) * kTB + tid;
         if (k0 + j < ntl && v < nv) {
           wt[j] = ld_stream_v4(trow + v);
           if (residual) wd[j] = ld_stream_v4(drow + v);
@@ -453,7 +456,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
       for (int j = 0; j < 4; ++j) {
         const int k = k0 + j;
         if (k < ntl) {  // block-uniform
-          const int v = k * kThreads + tid;
+          const int v = k * kTB + tid;
           float xt[VEC], xd[VEC], r[VEC];
           if (v < nv) {
             Staged<E>::unpack(wt[j], xt);
@@ -468,7 +471,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
           }
           const unsigned long long w = warp_sum_mass(
               vec_weight_scaled<VEC>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r));
-          if (lane == 0) tws[k * kWarps + warp] = w;
+          if (lane == 0) tws[k * kWB + warp] = w;
         }
       }
     }
@@ -476,7 +479,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
     if (rnd == 0) cluster_wait();  // every CTA of the cluster has started
     if (warp == 0) {
       unsigned long long t = 0;
-      for (int k = lane; k < ntl * kWarps; k += 32) t += tws[k];
+      for (int k = lane; k < ntl * kWB; k += 32) t += tws[k];
       t = warp_sum_u64(t);
       if (lane < C) *cluster.map_shared_rank(&s_mass[rnd][rank], lane) = t;
     }
@@ -503,10 +506,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
 
   int token = 0, near = 0;
   if (S != 0) {
-    double th = static_cast<double>(dec.uK) * static_cast<double>(S);
-    if (!(th >= 0.0)) th = 0.0;
-    const unsigned long long theta =
-        (th >= static_cast<double>(S)) ? S - 1 : static_cast<unsigned long long>(th);
+    const unsigned long long theta = draw_threshold(dec.uK, S);
     int cstar = C - 1;
     unsigned long long off = 0;
     for (int r = 0; r < C; ++r) {
@@ -523,7 +523,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
         const int k = k0 + lane;
         unsigned long long tt = 0;
         if (k < ntl)
-          for (int w = 0; w < kWarps; ++w) tt += tws[k * kWarps + w];
+          for (int w = 0; w < kWB; ++w) tt += tws[k * kWB + w];
         unsigned long long incl = tt;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -539,13 +539,20 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
         }
         base += __shfl_sync(0xffffffffu, incl, 31);
       }
-      int wstar = kWarps - 1;
-      for (int w = 0; w < kWarps; ++w) {
-        const unsigned long long m = tws[kstar * kWarps + w];
-        if (base + m > tl) { wstar = w; break; }
-        base += m;
+      int wstar = kWB - 1;
+      {  // the crossing warp of tile kstar: one lane per warp, scan and ballot
+        const unsigned long long m = lane < kWB ? tws[kstar * kWB + lane] : 0ull;
+        unsigned long long incl = m;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += o;
+        }
+        const unsigned int hit = __ballot_sync(0xffffffffu, lane < kWB && base + incl > tl);
+        if (hit) wstar = __ffs(hit) - 1;
+        base += __shfl_sync(0xffffffffu, incl - m, wstar);
       }
-      const int v = kstar * kThreads + wstar * 32 + lane;
+      const int v = kstar * kTB + wstar * 32 + lane;
       float xt[VEC], xd[VEC], r[VEC];
       if (v < nv) {
         Staged<E>::unpack(ld_stream_v4(trow + v), xt);
@@ -558,7 +565,8 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
 #pragma unroll
         for (int q = 0; q < VEC; ++q) xt[q] = xd[q] = -INFINITY;
       }
-      const unsigned long long w = vec_weight_scaled<VEC>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r);
+      const unsigned long long w =
+          vec_weight_scaled<VEC, true>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r);
       unsigned long long incl = w;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -576,14 +584,12 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
 #pragma unroll
         for (int k = 0; k < VEC; ++k) {
           acc = __fadd_rn(acc, r[k]);
-          const unsigned long long cc = __float2ull_rn(__fmul_rn(acc, kFix));
+          const unsigned long long cc = fix56(acc);
           if (cc > rem) { mstar = k; c_cur = cc; break; }
           c_prev = cc;
         }
         const long long t = (v0 + v) * VEC + mstar;
-        const double band = 1e-6 * static_cast<double>(S);
-        const bool nr = fabs(th - static_cast<double>(off + before + c_prev)) < band ||
-                        fabs(static_cast<double>(off + before + c_cur) - th) < band;
+        const bool nr = near_step(theta, off + before + c_prev, off + before + c_cur, S);
         int* dst = cluster.map_shared_rank(&s_tok[0], 0);
         dst[0] = static_cast<int>(t < a.V ? t : a.V - 1);
         dst[1] = nr ? 1 : 0;
@@ -607,10 +613,23 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   }
 }
 
-size_t smem_b(long long nvec, int C) {
+size_t smem_b(long long nvec, int C, int nt) {
   const long long nvs = (nvec + C - 1) / C;
-  const long long ntiles = (nvs + kThreads - 1) / kThreads;
-  return static_cast<size_t>(ntiles * kWarps * 8);
+  const long long ntiles = (nvs + nt - 1) / nt;
+  return static_cast<size_t>(ntiles * (nt / 32) * 8);
+}
+
+// Threads per CTA of kernel B: few clusters (few, long sequences) get larger
+// CTAs, so that every SM keeps as many slice loads in flight as when four
+// 256-thread CTAs share it -- provided all B clusters of that shape fit on the
+// GPU at once.
+int threads_b(long long B, int C, const DeviceInfo& dev) {
+  int c = 0;
+  while ((1 << c) < C && c < 3) ++c;
+  const long long ctas = B * C;
+  if (ctas <= dev.sm_count && B <= dev.decide_clusters[2][c]) return 1024;
+  if (ctas <= 2LL * dev.sm_count && B <= dev.decide_clusters[1][c]) return 512;
+  return kThreads;
 }
 
 constexpr int kSmemA = kStages2 * 2 * kChunk2 * 16;
@@ -623,18 +642,40 @@ constexpr int kSmemA = kStages2 * 2 * kChunk2 * 16;
 int sample_2p_cluster(long long nvec) {
   int C = 1;
   while (C < kMaxCB && (nvec + C - 1) / C > kSliceB) C *= 2;
-  return smem_b(nvec, C) <= 48 * 1024 ? C : 0;
+  return smem_b(nvec, C, kThreads) <= 48 * 1024 ? C : 0;
 }
 
-cudaError_t sample_2p_prepare(int* stream_ctas_per_sm) {
+cudaError_t sample_2p_prepare(DeviceInfo* d) {
   cudaError_t e = cudaFuncSetAttribute(norm_stream_kernel<BF16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemA);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(norm_stream_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemA);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(stream_ctas_per_sm, norm_stream_kernel<BF16>,
-                                                      kThreadsA, kSmemA);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d->stream_ctas_per_sm,
+                                                      norm_stream_kernel<BF16>, kThreadsA, kSmemA);
+  // how many clusters of kernel B fit at once, per (threads, cluster size)
+  for (int t = 0; t < 3 && e == cudaSuccess; ++t) {
+    for (int c = 0; c < 4 && e == cudaSuccess; ++c) {
+      const int nt = 256 << t, C = 1 << c;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned int>(C));
+      cfg.blockDim = dim3(nt);
+      cfg.dynamicSmemBytes = 4096;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = C;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = nt == 1024 ? cudaOccupancyMaxActiveClusters(&n, decide_sample_kernel<BF16, 1024>, &cfg)
+          : nt == 512 ? cudaOccupancyMaxActiveClusters(&n, decide_sample_kernel<BF16, 512>, &cfg)
+                      : cudaOccupancyMaxActiveClusters(&n, decide_sample_kernel<BF16, kThreads>, &cfg);
+      d->decide_clusters[t][c] = n;
+    }
+  }
   return e;
 }
 
@@ -671,8 +712,10 @@ cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned int>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_b(pt.nvec, C);
+  const int nt = threads_b(a.B, C, dev);
+  cfg.blockDim = dim3(nt);
+  cfg.dynamicSmemBytes = smem_b(pt.nvec, C, nt);
+  if (cfg.dynamicSmemBytes > 48 * 1024) return cudaErrorInvalidConfiguration;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -683,8 +726,14 @@ cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16>, a, pt)
-                : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32>, a, pt);
+  if (nt == 1024)
+    return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16, 1024>, a, pt)
+                  : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32, 1024>, a, pt);
+  if (nt == 512)
+    return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16, 512>, a, pt)
+                  : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32, 512>, a, pt);
+  return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16, kThreads>, a, pt)
+                : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32, kThreads>, a, pt);
 }
 
 }  // namespace specv

@@ -735,10 +735,7 @@ __device__ __noinline__ bool finish_draw(const VerifyArgs& a, const FusedGeom& g
   const int K = g.K, K1 = K + 1, b = j.b, n = j.n;
   int token = 0, near = 0;
   if (S != 0) {
-    double th = static_cast<double>(j.uK) * static_cast<double>(S);
-    if (!(th >= 0.0)) th = 0.0;
-    const unsigned long long theta =
-        (th >= static_cast<double>(S)) ? S - 1 : static_cast<unsigned long long>(th);
+    const unsigned long long theta = draw_threshold(j.uK, S);
     // the lane block holding the crossing, then the run inside it
     const int lb = __ffs(__ballot_sync(0xffffffffu, incl > theta)) - 1;
     unsigned long long base = __shfl_sync(0xffffffffu, incl - bs, lb);
@@ -773,7 +770,7 @@ __device__ __noinline__ bool finish_draw(const VerifyArgs& a, const FusedGeom& g
       }
     }
     const unsigned long long w =
-        vec_weight_scaled<VEC>(xt, xd, j.MSt, j.invZt, j.MSd, j.invZd, a.scale, residual, r);
+        vec_weight_scaled<VEC, true>(xt, xd, j.MSt, j.invZt, j.MSd, j.invZd, a.scale, residual, r);
     const unsigned long long wi = warp_scan_u64(w, lane);
     const unsigned int h3 = __ballot_sync(0xffffffffu, base + wi > theta);
     const int lstar = h3 ? __ffs(h3) - 1 : 31;
@@ -783,9 +780,7 @@ __device__ __noinline__ bool finish_draw(const VerifyArgs& a, const FusedGeom& g
       unsigned long long c_prev, c_cur;
       const int mstar = pick_in_vector<VEC>(r, w, theta - before, c_prev, c_cur);
       const long long t = v * VEC + mstar;
-      const double band = 1e-6 * static_cast<double>(S);
-      nr = (fabs(th - static_cast<double>(before + c_prev)) < band ||
-            fabs(static_cast<double>(before + c_cur) - th) < band) ? 1 : 0;
+      nr = near_step(theta, before + c_prev, before + c_cur, S) ? 1 : 0;
       tok = static_cast<int>(t < a.V ? t : a.V - 1);
     }
     token = __shfl_sync(0xffffffffu, tok, lstar);
