@@ -71,20 +71,19 @@ struct __align__(16) FusedCtl {
   unsigned long long done_ctas;  // CTAs that have taken their last unit
 };
 
-// Largest persistent grid of the two-kernel sampler's streaming pass.  Its
-// partials need at most kMaxStreamCtas + rows slots (contributor c of row pair
+// Most ranges the two-kernel sampler's streaming pass cuts the rows into.
+// Its partials need at most kMaxStreamCtas + rows slots (range c of row pair
 // p writes slot c + p).
 constexpr long long kMaxStreamCtas = 4096;
 
-// Workspace layout: SeqState[B] | units | float2 gathers[B*(K+1)] | FusedCtl,
-// 16-byte aligned parts, where `units` is RowSlot[B*(K+1)] (greedy kernel,
-// streaming sampler), Partial[B * tasks_per_seq] (fused sampler) or
-// Partial[kMaxStreamCtas + B*(K+1) + 1] (two-kernel sampler, which also uses
-// the gathers).  One call uses one view and leaves everything zero-filled,
-// so the views can share the region.  Sizes use 16-byte vectors of the row
-// (ceil(V*bytes/16)).
+// Workspace layout: SeqState[B] | units | FusedCtl, 16-byte aligned parts,
+// where `units` is RowSlot[B*(K+1)] (greedy kernel, streaming sampler),
+// Partial[B * tasks_per_seq] (fused sampler) or Partial[kMaxStreamCtas +
+// B*(K+1) + 1] (two-kernel sampler).  One call uses one view and leaves
+// everything zero-filled, so the views can share the region.  Sizes use
+// 16-byte vectors of the row (ceil(V*bytes/16)).
 struct WorkspaceLayout {
-  size_t seq, units, gathers, ctl, total;
+  size_t seq, units, ctl, total;
 };
 inline WorkspaceLayout workspace_layout(long long B, long long K, long long V, int elem_bytes) {
   const size_t R = (size_t)B * (size_t)(K + 1);
@@ -96,14 +95,34 @@ inline WorkspaceLayout workspace_layout(long long B, long long K, long long V, i
   size_t ub = R * sizeof(RowSlot);
   if (P * sizeof(Partial) > ub) ub = P * sizeof(Partial);
   if (((size_t)kMaxStreamCtas + R + 1) * sizeof(Partial) > ub) ub = ((size_t)kMaxStreamCtas + R + 1) * sizeof(Partial);
-  l.gathers = l.units + ub;
-  l.ctl = (l.gathers + R * 8 + 15) & ~(size_t)15;
+  l.ctl = (l.units + ub + 15) & ~(size_t)15;
   l.total = ((l.ctl + sizeof(FusedCtl)) + 255) & ~(size_t)255;
   return l;
 }
 inline size_t workspace_bytes(long long B, long long K, long long V, int elem_bytes) {
   return workspace_layout(B, K, V, elem_bytes).total;
 }
+
+// Division by a divisor fixed at launch, as one multiply-high: q = floor(n *
+// m / 2^64) with m = floor(2^64 / d) + 1 (2^64 / d when d is a power of two).
+// Writing m * d = 2^64 + e with 0 <= e <= d, the product is n / d + n*e /
+// (d * 2^64), whose floor is floor(n / d) whenever n * d < 2^64.  Every
+// quotient taken here has n * d < 2^60 for logits that fit in device memory.
+// (This GPU's 64-bit integer division is a ~500-cycle subroutine, its 32-bit
+// division ~140 cycles; a 64-bit multiply-high is ~40.)
+struct DivU64 {
+  unsigned long long m = 0;  // 0: divide by 1
+  static DivU64 make(unsigned long long d) {
+    DivU64 r;
+    r.m = d <= 1 ? 0ull : (~0ull / d) + 1ull;
+    return r;
+  }
+#ifdef __CUDACC__
+  __device__ __forceinline__ unsigned long long operator()(unsigned long long n) const {
+    return m ? __umul64hi(n, m) : n;
+  }
+#endif
+};
 
 #ifdef __CUDACC__
 
@@ -165,7 +184,7 @@ struct VecLoad<BF16, 1> {
   }
 };
 
-// One element of a row, as float (for the gathers t[x], d[x]).
+// One element of a row, as float (t[x], d[x] at a draft token x).
 template <typename E>
 __device__ __forceinline__ float load_one(const void* row, long long j);
 template <>

@@ -30,8 +30,7 @@ struct VerifyArgs {
   void* slots;                 // workspace: [B*(K+1)] RowSlot (greedy, streaming sampler)
   void* partials;              // workspace: Partial per work unit (fused sampler); same
                                // region as `slots`
-  void* ctl;                   // workspace: FusedCtl
-  void* gathers;               // workspace: [B*(K+1)] float2 (two-kernel sampler)
+  void* ctl;                   // workspace: FusedCtl (work counters)
 };
 
 // Per-device facts gathered once.

@@ -116,7 +116,6 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   a.slots = static_cast<char*>(workspace) + lay.units;
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
-  a.gathers = static_cast<char*>(workspace) + lay.gathers;
 
   const long long rows = static_cast<long long>(B) * (K + 1);
   if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;

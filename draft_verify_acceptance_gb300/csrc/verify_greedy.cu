@@ -132,13 +132,14 @@ __device__ __forceinline__ void thread_argmax_vec(const uint4* row, int v0, int 
 
 template <typename E, int VEC, int U>
 __global__ void __launch_bounds__(kThreads, 4)  // <= 64 registers: four CTAs per SM
-greedy_kernel(VerifyArgs a, int nvec, int S, bool one_word) {
-  // 32-bit index arithmetic: the grid fits int and nvec * S <= 2^22 * 64
+greedy_kernel(VerifyArgs a, int nvec, int S, DivU64 by_S, DivU64 by_K1, bool one_word) {
+  // 32-bit index arithmetic (the grid fits int and nvec * S <= 2^22 * 64);
+  // divisions by S and K + 1 as multiply-highs
   const int K1 = a.K + 1;
-  const int row = static_cast<int>(blockIdx.x) / S;
+  const int row = static_cast<int>(by_S(blockIdx.x));
   const int seg = static_cast<int>(blockIdx.x) - row * S;
-  const int v0 = nvec * seg / S;
-  const int v1 = nvec * (seg + 1) / S;
+  const int v0 = static_cast<int>(by_S(static_cast<unsigned long long>(nvec) * seg));
+  const int v1 = static_cast<int>(by_S(static_cast<unsigned long long>(nvec) * (seg + 1)));
   const char* base = static_cast<const char*>(a.target) +
                      static_cast<size_t>(row) * static_cast<size_t>(a.V) * E::kBytes;
 
@@ -146,7 +147,7 @@ greedy_kernel(VerifyArgs a, int nvec, int S, bool one_word) {
   // the draft token this row is compared with, fetched while the row streams
   int xtok = 0;
   if (one_word && tid == 0) {
-    const int b = row / K1, pos = row - b * K1;
+    const int b = static_cast<int>(by_K1(row)), pos = row - b * K1;
     if (pos < a.K) xtok = a.tokens[static_cast<size_t>(b) * a.K + pos];
   }
 
@@ -203,7 +204,7 @@ greedy_kernel(VerifyArgs a, int nvec, int S, bool one_word) {
     const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
     key = o > key ? o : key;
   }
-  const int b = row / K1;
+  const int b = static_cast<int>(by_K1(row));
 
   if (one_word) {  // one CTA per row: g_i to its slot, one atomic on the sequence
     if (lane == 0) {
@@ -300,7 +301,9 @@ cudaError_t launch_greedy_t(const VerifyArgs& a, const DeviceInfo& dev, cudaStre
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   const bool one_word = S == 1 && a.K + 1 <= kOneWordRows;
-  return cudaLaunchKernelEx(&cfg, greedy_kernel<E, VEC, U>, a, static_cast<int>(nvec), S, one_word);
+  return cudaLaunchKernelEx(&cfg, greedy_kernel<E, VEC, U>, a, static_cast<int>(nvec), S,
+                            DivU64::make(static_cast<unsigned long long>(S)),
+                            DivU64::make(static_cast<unsigned long long>(a.K + 1)), one_word);
 }
 
 }  // namespace

@@ -46,24 +46,38 @@ namespace specv {
 // Byte-weighted partition of the pair-vector space over G CTAs.  Vectors
 // [0, P) belong to draft pairs (positions 0..K-1, weight 2), [P, P + Q) to
 // bonus rows (position K, weight 1); pair p = i*B + b covers vectors
-// [p*nvec, (p+1)*nvec).
+// [p*nvec, (p+1)*nvec).  CTA c streams the weight range [W*c/G, W*(c+1)/G).
+// (Handing out smaller ranges dynamically was measured: it evens out the
+// CTAs' finishing times but not the last one, since the pass is bound by the
+// GPU's total throughput, not by its slowest CTA.)
 struct StreamPartition {
   long long nvec, P, Q, W;
   int G;
-  __host__ __device__ long long vec_of_w(long long w) const {
-    return w <= 2 * P ? w / 2 : P + (w - 2 * P);
+  // launch-time constants of the division-free index arithmetic: W = qw*G + rw
+  long long qw;
+  int rw;
+  float fw;                                // G / W (estimate)
+  DivU64 by_G, by_nvec, by_B;
+  __device__ long long vec_of_w(long long w) const {
+    return w <= 2 * P ? (w >> 1) : P + (w - 2 * P);
   }
-  __host__ __device__ long long w_of_vec(long long v) const {
+  __device__ long long w_of_vec(long long v) const {
     return v <= P ? 2 * v : 2 * P + (v - P);
   }
-  // first vector of CTA c (c = G gives the end)
-  __host__ __device__ long long lo(int c) const {
-    return c >= G ? P + Q : vec_of_w(W * c / G);
+  // first vector of CTA c (c = G gives the end): weight floor(W*c/G)
+  __device__ long long lo(int c) const {
+    if (c >= G) return P + Q;
+    return vec_of_w(qw * c + static_cast<long long>(by_G(static_cast<unsigned long long>(rw) * c)));
   }
-  // the CTA whose range holds vector v: the largest c with lo(c) <= v
-  __host__ __device__ int cta_of(long long v) const {
-    const long long c = (w_of_vec(v + 1) * G - 1) / W;
-    return static_cast<int>(c < G - 1 ? c : G - 1);
+  // the CTA whose range holds vector v: the largest c with lo(c) <= v (a
+  // float estimate, corrected against lo())
+  __device__ int cta_of(long long v) const {
+    const long long w1 = w_of_vec(v + 1);  // lo(c) <= v  <=>  start weight of c < w1
+    int c = static_cast<int>(static_cast<float>(w1 - 1) * fw);
+    c = c < 0 ? 0 : (c > G - 1 ? G - 1 : c);
+    while (c > 0 && lo(c) > v) --c;
+    while (c + 1 < G && lo(c + 1) <= v) ++c;
+    return c;
   }
 };
 
@@ -79,11 +93,11 @@ constexpr int kMaxPending2 = 32;
 struct PairCursor {
   long long pos, hi, nvec, pair_end;
   int i, b, B;
-  __device__ PairCursor(long long lo, long long hi_, long long nvec_, int B_)
-      : pos(lo), hi(hi_), nvec(nvec_), B(B_) {
-    const long long p = lo / nvec_;
-    pair_end = (p + 1) * nvec_;
-    i = static_cast<int>(p / B_);
+  __device__ PairCursor(long long lo, long long hi_, const StreamPartition& pt, int B_)
+      : pos(lo), hi(hi_), nvec(pt.nvec), B(B_) {
+    const long long p = static_cast<long long>(pt.by_nvec(lo));
+    pair_end = (p + 1) * nvec;
+    i = static_cast<int>(pt.by_B(p));
     b = static_cast<int>(p - static_cast<long long>(i) * B_);
   }
   // next chunk: start, length, the pair's (i, b) and the offset in the pair.
@@ -130,20 +144,13 @@ __device__ __forceinline__ void issue_chunk(const VerifyArgs& a, long long nvec,
   }
 }
 
-// The draft token of pair (i, b) (clamped into the vocabulary), or -1 for a
-// bonus row or past the end.
-__device__ __forceinline__ int pair_token(const VerifyArgs& a, int i, int b) {
-  if (i >= a.K) return -1;
-  const int x = __ldg(a.tokens + static_cast<size_t>(b) * a.K + i);
-  return min(max(x, 0), a.V - 1);
-}
-
 constexpr int kThreadsA = kThreads + 32;  // 8 consumer warps + 1 producer warp
 
 // Consumer warps only (named barrier 1): warp 0 merges the parked partials of
-// each pair over the 8 warps and stores one Partial per (CTA, pair).
-__device__ __forceinline__ void flush_partials(Partial* partials, int c, const float4* s_pend,
-                                               const long long* s_pair, int npend, int warp,
+// each (range, pair) over the 8 warps and stores one Partial at its slot
+// (range + pair).
+__device__ __forceinline__ void flush_partials(Partial* partials, const float4* s_pend,
+                                               const long long* s_slot, int npend, int warp,
                                                int lane) {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
   if (warp == 0) {
@@ -156,7 +163,7 @@ __device__ __forceinline__ void flush_partials(Partial* partials, int c, const f
       }
       Partial out;
       out.ms_t = v.x; out.z_t = v.y; out.ms_d = v.z; out.z_d = v.w;
-      partials[c + s_pair[j]] = out;
+      partials[s_slot[j]] = out;
     }
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
@@ -170,7 +177,7 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
   extern __shared__ __align__(128) uint4 ring2[];  // [kStages2][target, draft][kChunk2]
   __shared__ __align__(8) unsigned long long full[kStages2];   // copies landed
   __shared__ __align__(8) unsigned long long empty[kStages2];  // consumers done
-  __shared__ long long s_pair[kMaxPending2];
+  __shared__ long long s_slot[kMaxPending2];  // partial slot (range + pair) of each parked entry
   __shared__ float4 s_pend[kMaxPending2 * kWarps];
 
   // the decide-and-sample kernel may be scheduled as soon as SMs free up;
@@ -195,7 +202,7 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
   // ---- producer warp: one thread keeps kStages2 chunks in flight ---------
   if (warp == kWarps) {
     if (lane == 0) {
-      PairCursor prod(vlo, vhi, nvec, a.B);
+      PairCursor prod(vlo, vhi, pt, a.B);
       bool ok = true;
       long long st, off;
       int len, pi, pb;
@@ -213,16 +220,12 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
   // ---- consumer warps -----------------------------------------------------
   // Per-pair facts are set once per pair; per chunk only 32-bit arithmetic.
   Partial* partials = static_cast<Partial*>(a.partials);
-  float2* gathers = static_cast<float2*>(a.gathers);
   long long pos = vlo;
-  long long p = vlo / nvec;                 // current pair
-  long long pair_end = (p + 1) * nvec;      // its end in the flat space
-  int in_pair = static_cast<int>(vlo - p * nvec);  // vectors of the pair before pos
-  int ci = static_cast<int>(p / a.B);       // (position, sequence) of pair p
+  long long p = static_cast<long long>(pt.by_nvec(vlo));  // current pair
+  long long pair_end = (p + 1) * nvec;                     // its end in the flat space
+  int in_pair = static_cast<int>(vlo - p * nvec);          // vectors of the pair before pos
+  int ci = static_cast<int>(pt.by_B(p));                   // (position, sequence) of pair p
   int cb = static_cast<int>(p - static_cast<long long>(ci) * a.B);
-  const int nb = cb + 1 == a.B ? 0 : cb + 1, ni = cb + 1 == a.B ? ci + 1 : ci;
-  int x_cur = pair_token(a, ci, cb);        // clamped token, or -1 for a bonus row
-  int x_nxt = pair_token(a, ni, nb);        // prefetched for the next pair
   int npend = 0;
   RowAcc At{-INFINITY, 0.f}, Ad{-INFINITY, 0.f};
   bool ok = true;
@@ -233,9 +236,9 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
       warp_merge_scaled(mt, zt);
       warp_merge_scaled(md, zd);
       if (lane == 0) s_pend[npend * kWarps + warp] = make_float4(mt, zt, md, zd);
-      if (tid == 0) s_pair[npend] = p;
+      if (tid == 0) s_slot[npend] = c + p;
       if (++npend == kMaxPending2) {
-        flush_partials(partials, c, s_pend, s_pair, npend, warp, lane);
+        flush_partials(partials, s_pend, s_slot, npend, warp, lane);
         npend = 0;
       }
       ++p;
@@ -245,12 +248,10 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
         cb = 0;
         ++ci;
       }
-      x_cur = x_nxt;
-      x_nxt = cb + 1 == a.B ? pair_token(a, ci + 1, 0) : pair_token(a, ci, cb + 1);
       At = RowAcc{-INFINITY, 0.f};
       Ad = RowAcc{-INFINITY, 0.f};
     }
-    const bool has_draft = x_cur >= 0;
+    const bool has_draft = ci < a.K;  // a (target, draft) pair, else a bonus row
     long long end = pos + (has_draft ? kChunk2 : 2 * kChunk2);
     if (end > vhi) end = vhi;
     if (end > pair_end) end = pair_end;
@@ -270,14 +271,6 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
     if (nvalid > 1) wt[1] = stage_t[tid + kThreads];
     if (nvalid2 > 0) wd[0] = stage_d[tid];
     if (nvalid2 > 1) wd[1] = stage_d[tid + kThreads];
-    if (has_draft) {
-      // the thread holding x_i's vector records t[x_i], d[x_i]
-      const int lv = x_cur / VEC - in_pair;
-      if (lv >= 0 && lv < len && (lv & (kThreads - 1)) == tid) {
-        const int j = lv * VEC + x_cur % VEC;
-        gathers[p] = make_float2(staged_elem<E>(stage_t, j), staged_elem<E>(stage_d, j));
-      }
-    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[q]);  // this warp is done reading stage q
     acc_vectors<E>(At, wt, nvalid, s);
@@ -290,15 +283,25 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
     warp_merge_scaled(mt, zt);
     warp_merge_scaled(md, zd);
     if (lane == 0) s_pend[npend * kWarps + warp] = make_float4(mt, zt, md, zd);
-    if (tid == 0) s_pair[npend] = p;
+    if (tid == 0) s_slot[npend] = c + p;
     ++npend;
   }
-  flush_partials(partials, c, s_pend, s_pair, npend, warp, lane);
+  flush_partials(partials, s_pend, s_slot, npend, warp, lane);
   if (!ok && a.status) atomicOr(a.status, kWaitTimeout);
 }
 
 constexpr int kMaxCB = 8;                // largest cluster of kernel B
+constexpr int kMaxK1 = 65;               // K + 1 <= 65 (the API's largest K is 64)
 constexpr int kSliceB = 2048;            // vectors per row that one CTA of kernel B aims for
+
+// t[b, i, x] and d[b, i, x] (x clamped into the vocabulary) as fp32.
+template <typename E>
+__device__ __forceinline__ float2 logits_at(const VerifyArgs& a, int b, int i, int x) {
+  const long long xc = min(max(x, 0), a.V - 1);
+  const long long ti = (static_cast<long long>(b) * (a.K + 1) + i) * a.V + xc;
+  const long long di = (static_cast<long long>(b) * a.K + i) * a.V + xc;
+  return make_float2(load_one<E>(a.target, ti), load_one<E>(a.draft, di));
+}
 
 // Decision of one sequence, pushed from rank 0 to every CTA of its cluster.
 struct Decision {
@@ -317,7 +320,8 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  const int b = static_cast<int>(blockIdx.x / C);
+  const int lgC = __ffs(C) - 1;  // C is a power of two
+  const int b = static_cast<int>(blockIdx.x >> lgC);
   const int K = a.K, K1 = K + 1;
   const long long nvec = pt.nvec;
   const float s = a.scale;
@@ -327,19 +331,75 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   __shared__ Decision s_dec;                           // this CTA's decision
   __shared__ unsigned long long s_mass[2][kMaxCB];     // pushed by each rank
   __shared__ int s_tok[2];                             // pushed by the crossing CTA to rank 0
+  __shared__ float4 s_norm[kMaxK1];                    // per position: (MSt, Zt, MSd, Zd)
 
   cluster_arrive_relaxed();  // matched by cluster_wait() before the first DSMEM push
+
+  // The call's inputs are complete before the normaliser stream starts, so
+  // warp 0 reads the first 32 positions' uniforms, draft tokens and the two
+  // logits at each token now, while the stream may still be running.
+  const float* u = a.uniforms + static_cast<size_t>(b) * K1;
+  float2 g0 = make_float2(0.f, 0.f);
+  int x0 = 0;
+  float u0 = 0.f;
+  if (warp == 0 && lane <= K) {
+    u0 = u[lane];
+    if (lane < K) {
+      x0 = a.tokens[static_cast<size_t>(b) * K + lane];
+      g0 = logits_at<E>(a, b, lane, x0);
+    }
+  }
+
   // everything below reads what the normaliser stream wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  // ---- row normalisers (all warps; identical in every CTA) --------------
+  // Warp w merges positions w, w + kWB, ...: one lane per contributing range
+  // (the loads of up to four positions in flight at once), then a butterfly.
+  const Partial* partials = static_cast<const Partial*>(a.partials);
+  for (int i0 = warp; i0 <= K; i0 += 4 * kWB) {
+    Partial q[4];
+    int f[4], l[4];
+    long long pp[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = i0 + t * kWB;
+      q[t] = Partial{-INFINITY, 0.f, -INFINITY, 0.f};
+      f[t] = 0;
+      l[t] = -1;
+      pp[t] = 0;
+      if (i <= K) {
+        pp[t] = static_cast<long long>(i) * a.B + b;
+        f[t] = pt.cta_of(pp[t] * nvec);
+        l[t] = pt.cta_of((pp[t] + 1) * nvec - 1);
+        if (f[t] + lane <= l[t]) q[t] = partials[f[t] + lane + pp[t]];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = i0 + t * kWB;
+      if (i <= K) {  // warp-uniform
+        float mt = q[t].ms_t, zt = q[t].z_t, md = q[t].ms_d, zd = q[t].z_d;
+        warp_merge_scaled(mt, zt);
+        warp_merge_scaled(md, zd);
+        for (int j0 = f[t] + 32; j0 <= l[t]; j0 += 32) {  // rows over more than 32 ranges
+          Partial r = Partial{-INFINITY, 0.f, -INFINITY, 0.f};
+          if (j0 + lane <= l[t]) r = partials[j0 + lane + pp[t]];
+          warp_merge_scaled(r.ms_t, r.z_t);
+          warp_merge_scaled(r.ms_d, r.z_d);
+          merge_scaled(mt, zt, r.ms_t, r.z_t);
+          merge_scaled(md, zd, r.ms_d, r.z_d);
+        }
+        if (lane == 0) s_norm[i] = make_float4(mt, zt, md, zd);
+      }
+    }
+  }
+  __syncthreads();
+
   // ---- decision (warp 0 of every CTA; identical in all of them) ----------
-  // One lane per position: all loads first, then the merge in contributor
-  // order and the ratio test; a ballot gives the first rejection n.  Only
-  // rank 0 writes p(x_i), q(x_i) and the status.
+  // One lane per position: the ratio test, then a ballot gives the first
+  // rejection n.  Only rank 0 writes p(x_i), q(x_i) and the status.
   if (warp == 0) {
-    const Partial* partials = static_cast<const Partial*>(a.partials);
-    const float2* gathers = static_cast<const float2*>(a.gathers);
-    const float* u = a.uniforms + static_cast<size_t>(b) * K1;
     const bool writer = rank == 0;
     int n = K, bad = 0, ratio_near = 0;
     float nMSt = 0.f, nZt = 0.f, nMSd = 0.f, nZd = 0.f;
@@ -348,31 +408,17 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
       float MSt = -INFINITY, Zt = 0.f, MSd = -INFINITY, Zd = 0.f;
       bool rej = false, nr = false;
       if (i <= K) {
-        const long long p = static_cast<long long>(i) * a.B + b;
-        const int f = pt.cta_of(p * nvec), l = pt.cta_of((p + 1) * nvec - 1);
-        const int nc = l - f + 1;
-        Partial qa[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (j < nc) qa[j] = partials[f + j + p];
-        float2 g = make_float2(0.f, 0.f);
-        int xr = 0;
-        if (i < K) {
-          g = gathers[p];
-          xr = a.tokens[static_cast<size_t>(b) * K + i];
-        }
-        const float ui = u[i];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (j < nc) {
-            merge_scaled(MSt, Zt, qa[j].ms_t, qa[j].z_t);
-            merge_scaled(MSd, Zd, qa[j].ms_d, qa[j].z_d);
+        const float4 nz = s_norm[i];
+        MSt = nz.x; Zt = nz.y; MSd = nz.z; Zd = nz.w;
+        float2 g = g0;
+        int xr = x0;
+        float ui = u0;
+        if (i0 > 0) {
+          ui = u[i];
+          if (i < K) {
+            xr = a.tokens[static_cast<size_t>(b) * K + i];
+            g = logits_at<E>(a, b, i, xr);
           }
-        }
-        for (int j = 4; j < nc; ++j) {  // rows spread over many CTAs (small B*K)
-          const Partial q = partials[f + j + p];
-          merge_scaled(MSt, Zt, q.ms_t, q.z_t);
-          merge_scaled(MSd, Zd, q.ms_d, q.z_d);
         }
         if (!(isfinite(MSt) && isfinite(Zt) && Zt > 0.f)) bad |= kDataNonfiniteLogit;
         if (!(ui >= 0.f && ui < 1.f)) bad |= kDataUniformRange;
@@ -427,8 +473,8 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   const Decision dec = s_dec;
   const int n = dec.n;
   bool residual = n < K;
-  const long long v0 = nvec * rank / C;
-  const int nv = static_cast<int>(nvec * (rank + 1) / C - v0);
+  const long long v0 = (nvec * rank) >> lgC;
+  const int nv = static_cast<int>(((nvec * (rank + 1)) >> lgC) - v0);
   const int ntl = (nv + kTB - 1) / kTB;
   const uint4* trow = static_cast<const uint4*>(a.target) + (static_cast<size_t>(b) * K1 + n) * nvec + v0;
   const uint4* drow = residual
@@ -490,17 +536,15 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
     residual = false;  // p == q at this row: the draw falls back to p
   }
 
-  // every CTA of the cluster has read the partials and gathers (they were
-  // read before the first cluster barrier): rank 0 puts its sequence's slots back
-  // to zero, keeping the workspace zero-filled between calls
+  // every CTA of the cluster has read the partials (before the first cluster
+  // barrier): rank 0 puts its sequence's slots back to zero, keeping the
+  // workspace zero-filled between calls
   if (rank == 0 && warp == 0) {
     Partial* partials = static_cast<Partial*>(a.partials);
-    float2* gathers = static_cast<float2*>(a.gathers);
     for (int i = lane; i <= K; i += 32) {
       const long long p = static_cast<long long>(i) * a.B + b;
       const int f = pt.cta_of(p * nvec), l = pt.cta_of((p + 1) * nvec - 1);
       for (int c = f; c <= l; ++c) partials[c + p] = Partial{0.f, 0.f, 0.f, 0.f};
-      if (i < K) gathers[p] = make_float2(0.f, 0.f);
     }
   }
 
@@ -692,6 +736,12 @@ StreamPartition stream_partition(const VerifyArgs& a, const DeviceInfo& dev) {
   if (G > pt.W / 4) G = pt.W / 4;  // every CTA owns at least one vector
   if (G < 1) G = 1;
   pt.G = static_cast<int>(G);
+  pt.qw = pt.W / G;
+  pt.rw = static_cast<int>(pt.W % G);
+  pt.fw = static_cast<float>(static_cast<double>(G) / static_cast<double>(pt.W));
+  pt.by_G = DivU64::make(static_cast<unsigned long long>(G));
+  pt.by_nvec = DivU64::make(static_cast<unsigned long long>(pt.nvec));
+  pt.by_B = DivU64::make(static_cast<unsigned long long>(a.B));
   return pt;
 }
 

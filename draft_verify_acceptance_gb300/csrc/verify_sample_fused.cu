@@ -130,6 +130,7 @@ struct FusedGeom {
   int ne;           // 32-vector runs per row
   int K, B;
   long long total;  // B * tps
+  DivU64 by_tps, by_segs;  // divisions by tps and segs as multiply-highs
 };
 
 template <typename T>
@@ -256,12 +257,12 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
         continue;
       }
       have_next = false;
-      const long long b = static_cast<long long>(t / static_cast<unsigned long long>(g.tps));
+      const long long b = static_cast<long long>(g.by_tps(t));
       const int jj = static_cast<int>(static_cast<long long>(t) - b * g.tps);
       cb = static_cast<int>(b);
       int i, coff;
       if (jj < K * g.segs) {
-        i = jj / g.segs;
+        i = static_cast<int>(g.by_segs(static_cast<unsigned long long>(jj)));
         coff = (jj - i * g.segs) * kFusedSeg;
         cend = min(coff + kFusedSeg, nvec);
         cdrow = D + (static_cast<size_t>(cb) * K + i) * nvec;
@@ -955,6 +956,8 @@ cudaError_t launch_sample_fused(const VerifyArgs& a, const DeviceInfo& dev, cuda
   g.K = a.K;
   g.B = a.B;
   g.total = static_cast<long long>(a.B) * g.tps;
+  g.by_tps = DivU64::make(static_cast<unsigned long long>(g.tps));
+  g.by_segs = DivU64::make(static_cast<unsigned long long>(g.segs));
   long long G = dev.sm_count > 0 ? dev.sm_count : 1;
   if (G > g.total) G = g.total;
   FusedCtl* ctl = static_cast<FusedCtl*>(a.ctl);
