@@ -267,14 +267,25 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
     const int nvalid = (tid < half ? 1 : 0) + (tid + kThreads < half ? 1 : 0);
     const int nvalid2 = (tid < rest ? 1 : 0) + (tid + kThreads < rest ? 1 : 0);
     uint4 wt[2], wd[2];
-    if (nvalid > 0) wt[0] = stage_t[tid];
-    if (nvalid > 1) wt[1] = stage_t[tid + kThreads];
-    if (nvalid2 > 0) wd[0] = stage_d[tid];
-    if (nvalid2 > 1) wd[1] = stage_d[tid + kThreads];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[q]);  // this warp is done reading stage q
-    acc_vectors<E>(At, wt, nvalid, s);
-    acc_vectors<E>(has_draft ? Ad : At, wd, nvalid2, s);
+    if (rest == kChunk2) {  // a full stage (block-uniform): no per-element selects
+      wt[0] = stage_t[tid];
+      wt[1] = stage_t[tid + kThreads];
+      wd[0] = stage_d[tid];
+      wd[1] = stage_d[tid + kThreads];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[q]);  // this warp is done reading stage q
+      acc_vectors_full<E>(At, wt, s);
+      acc_vectors_full<E>(has_draft ? Ad : At, wd, s);
+    } else {
+      if (nvalid > 0) wt[0] = stage_t[tid];
+      if (nvalid > 1) wt[1] = stage_t[tid + kThreads];
+      if (nvalid2 > 0) wd[0] = stage_d[tid];
+      if (nvalid2 > 1) wd[1] = stage_d[tid + kThreads];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[q]);
+      acc_vectors<E>(At, wt, nvalid, s);
+      acc_vectors<E>(has_draft ? Ad : At, wd, nvalid2, s);
+    }
     pos = end;
     in_pair += len;
   }
