@@ -360,6 +360,16 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long
   return old;
 }
 
+__device__ __forceinline__ void red_add_release_gpu(unsigned int* p, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ bool arrive_last(SeqState* seq, int b, unsigned int total) {
   return atom_add_acq_rel_gpu(&seq[b].arrivals, 1u) + 1u == total;
 }

@@ -17,13 +17,17 @@
 // segments of kFusedSeg 16-byte vectors and the bonus target row into
 // segments of twice that; units are numbered sequence-major, so at any moment
 // the GPU works on a narrow window of consecutive sequences.  One CTA runs on
-// each SM and takes units from a global counter as it goes, so a CTA that
-// spends time on a draw simply takes fewer units.
+// each SM (a cooperative launch: all of them resident) and takes units from a
+// global counter as it goes, so a CTA that spends time on a draw simply takes
+// fewer units.  Sequence b is decided and drawn by CTA b mod grid, whichever
+// CTAs streamed it: the draws are spread evenly and never pile up on the CTAs
+// that happen to finish sequences.
 //
 // Warp roles in a CTA:
-//   producer (one thread): claims units and moves their rows into a ring of
-//     shared-memory stages with cp.async.bulk, and on request moves the row
-//     pair of a decided sequence through the same ring;
+//   producer (one thread): claims units (one ahead) and moves their rows into
+//     a ring of shared-memory stages with cp.async.bulk, and on request moves
+//     the row pair of a decided sequence through the same ring, ahead of the
+//     next unit;
 //   16 consumer warps: per stage, online normalisers (max and sum of
 //     2^(x*s - offset)) of the target and draft segment; at a unit's end each
 //     warp folds its lanes and leaves one value per warp.  For a draw stage
@@ -32,15 +36,17 @@
 //     another or on the other roles, only on the ring;
 //   arrivals (one warp): folds the 16 warp values of each unit in a fixed
 //     order, writes the unit's Partial to the workspace and counts it on its
-//     sequence with an acquire-release atomic, many units per round trip; a
-//     count that completes a sequence is handed on;
-//   decisions (one warp): for each sequence this CTA completed, merges the
-//     sequence's partials row by row in unit order, runs the K accept tests,
-//     finds the first rejection n and asks the producer for row pair n (or
-//     the bonus row), which is still in L2.  When the consumers have reduced
-//     it, the warp locates the crossing run of the inverse CDF, recomputes
-//     that run's 32 vectors from global memory and writes the outputs.
-// Nothing waits on another CTA; within a CTA every wait is bounded.
+//     sequence with a release add (no round trip);
+//   decisions (one warp): for each of its sequences (b = blockIdx.x, + grid,
+//     ...), waits with an acquire load until all of the sequence's units are
+//     counted, merges its partials row by row in unit order, runs the K
+//     accept tests, finds the first rejection n and asks the producer for row
+//     pair n (or the bonus row), streamed moments ago.  When the consumers
+//     have reduced it, the warp locates the crossing run of the inverse CDF,
+//     recomputes that run's 32 vectors from global memory and writes the
+//     outputs.
+// Only the decision warp waits on other CTAs (their unit counts), and the
+// cooperative launch guarantees those CTAs are running; every wait is bounded.
 #include <climits>
 
 #include "device_common.cuh"
@@ -63,20 +69,15 @@ constexpr int kMaxEntries = static_cast<int>(kFusedMaxVec / 32);  // 32-vector r
 constexpr int kScratch = 512;               // partials per decision window
 constexpr int kPartBuf = 16;                // unit ends the consumers may run ahead
 constexpr int kUQ = 64;                     // producer -> arrivals: units issued
-constexpr int kDQ = 64;                     // arrivals -> decisions: completed sequences
 constexpr int kBatch = 8;                   // unit ends the arrival warp takes at once
 constexpr int kRounds = (64 + 1 + 31) / 32; // rows per lane in a decision (K <= 64)
 constexpr unsigned int kMaxIdle = 1u << 22;
 // Decisions -> producer draw requests.  At most 2 are issued and unfinished
-// (two run-mass tables).  While a completed sequence or a request waits, the
-// producer claims no unit, so the only other sequences that can still
-// complete here are those of units already issued (ring, in issue, claimed
-// ahead) and of ends not yet folded (kPartBuf).
+// (two run-mass tables); the decision warp posts at most one request per
+// sequence it owns.
 constexpr int kReq = 64;
 static_assert(kFusedSeg % kLs == 0, "a pair segment is a whole number of stages");
 static_assert(kBatch <= kPartBuf, "batched tests must not alias");
-static_assert(kReq > 2 + 1 + kStagesF + 2 + kPartBuf, "outstanding draw requests fit");
-static_assert(kDQ > 1 + kStagesF + 2 + kPartBuf, "completed sequences fit");
 static_assert(kUQ > kStagesF + 2 + kPartBuf, "issued units fit");
 
 constexpr size_t kSmemF = static_cast<size_t>(kStagesF) * kStageVec * 16 +
@@ -109,16 +110,13 @@ struct FusedShared {
   unsigned long long full[kStagesF], empty[kStagesF];
   unsigned long long part_full[kPartBuf], part_free[kPartBuf];
   unsigned long long drawn[2];                // a draw's run masses are all in its table
-  unsigned long long dq_full[kDQ], dq_empty[kDQ];
   StageInfo info[kStagesF];
   float4 part[kPartBuf][kCW];                 // one value per consumer warp per unit end
   long long utau[kUQ];                        // units in issue order
   int ub[kUQ];
-  int dq_b[kDQ];                              // completed sequence, or -1 once all are done
   Job jobs[kReq];
   long long units_issued, units_final, units_folded;  // units_final: -1 until known
   long long req_posted, draws_finished;       // written by the decision warp
-  long long seq_pushed, seq_taken;            // completed sequences handed on / taken
   int exit_flag, abort_flag;
 };
 
@@ -202,7 +200,7 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
   const uint4* ctrow = nullptr;
   const uint4* cdrow = nullptr;
   int cb = 0, cend = 0, cnext = 0;
-  // one unit is claimed ahead of its use, unless a decision is pending
+  // one unit is claimed ahead of its use
   unsigned long long next = atomicAdd(&ctl->next_task, 1ull);
   bool have_next = true;
   unsigned int idle = 0;
@@ -232,62 +230,8 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
     }
     const long long posted = vld(sh.req_posted);
     const bool want_draw = posted > taken;
-    // a completed sequence not yet decided, or a draw not yet issued: claim
-    // nothing new, so this CTA's other units are not held up behind the draw
-    const bool busy = want_draw || vld(sh.seq_pushed) > vld(sh.seq_taken);
-    if (have_next) {  // start the unit claimed ahead
-      const unsigned long long t = next;
-      if (t >= static_cast<unsigned long long>(g.total)) {
-        have_next = false;
-        exhausted = true;
-        vst(sh.units_final, units);
-        // the last CTA to take its final unit puts the counters back to zero
-        if (atomicAdd(&ctl->done_ctas, 1ull) == static_cast<unsigned long long>(gridDim.x) - 1ull) {
-          ctl->next_task = 0ull;
-          ctl->done_ctas = 0ull;
-        }
-        continue;
-      }
-      if (units - vld(sh.units_folded) >= kUQ) {  // cannot happen (see kUQ)
-        if (++idle > kMaxIdle) {
-          ok = false;
-          break;
-        }
-        __nanosleep(64);
-        continue;
-      }
-      have_next = false;
-      const long long b = static_cast<long long>(g.by_tps(t));
-      const int jj = static_cast<int>(static_cast<long long>(t) - b * g.tps);
-      cb = static_cast<int>(b);
-      int i, coff;
-      if (jj < K * g.segs) {
-        i = static_cast<int>(g.by_segs(static_cast<unsigned long long>(jj)));
-        coff = (jj - i * g.segs) * kFusedSeg;
-        cend = min(coff + kFusedSeg, nvec);
-        cdrow = D + (static_cast<size_t>(cb) * K + i) * nvec;
-      } else {
-        i = K;
-        coff = (jj - K * g.segs) * 2 * kFusedSeg;
-        cend = min(coff + 2 * kFusedSeg, nvec);
-        cdrow = nullptr;
-      }
-      ctrow = T + (static_cast<size_t>(cb) * (K + 1) + i) * nvec;
-      cnext = coff;
-      in_unit = true;
-      // tell the arrival warp which unit ends next
-      sh.ub[units % kUQ] = cb;
-      sh.utau[units % kUQ] = static_cast<long long>(t);
-      __threadfence_block();
-      vst(sh.units_issued, ++units);
-      if (!busy) {
-        next = atomicAdd(&ctl->next_task, 1ull);
-        have_next = true;
-      }
-      idle = 0;
-      continue;
-    }
-    // request `taken` uses table taken & 1, free once request taken-2 is done
+    // a requested draw goes ahead of the next unit; request `taken` uses
+    // table taken & 1, free once request taken-2 is done
     if (want_draw && (taken < 2 || vld(sh.draws_finished) >= taken - 1)) {
       __threadfence_block();
       const Job j = sh.jobs[taken % kReq];
@@ -320,9 +264,54 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
       idle = 0;
       continue;
     }
-    if (!busy && !exhausted) {  // claim the next unit
-      next = atomicAdd(&ctl->next_task, 1ull);
+    if (have_next) {  // start the unit claimed ahead
+      const unsigned long long t = next;
+      if (t >= static_cast<unsigned long long>(g.total)) {
+        have_next = false;
+        exhausted = true;
+        vst(sh.units_final, units);
+        // the last CTA to take its final unit puts the counters back to zero
+        if (atomicAdd(&ctl->done_ctas, 1ull) == static_cast<unsigned long long>(gridDim.x) - 1ull) {
+          ctl->next_task = 0ull;
+          ctl->done_ctas = 0ull;
+        }
+        continue;
+      }
+      if (units - vld(sh.units_folded) >= kUQ) {  // the arrival warp is kUQ units behind
+        if (++idle > kMaxIdle) {
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
+        continue;
+      }
+      have_next = false;
+      const long long b = static_cast<long long>(g.by_tps(t));
+      const int jj = static_cast<int>(static_cast<long long>(t) - b * g.tps);
+      cb = static_cast<int>(b);
+      int i, coff;
+      if (jj < K * g.segs) {
+        i = static_cast<int>(g.by_segs(static_cast<unsigned long long>(jj)));
+        coff = (jj - i * g.segs) * kFusedSeg;
+        cend = min(coff + kFusedSeg, nvec);
+        cdrow = D + (static_cast<size_t>(cb) * K + i) * nvec;
+      } else {
+        i = K;
+        coff = (jj - K * g.segs) * 2 * kFusedSeg;
+        cend = min(coff + 2 * kFusedSeg, nvec);
+        cdrow = nullptr;
+      }
+      ctrow = T + (static_cast<size_t>(cb) * (K + 1) + i) * nvec;
+      cnext = coff;
+      in_unit = true;
+      // tell the arrival warp which unit ends next
+      sh.ub[units % kUQ] = cb;
+      sh.utau[units % kUQ] = static_cast<long long>(t);
+      __threadfence_block();
+      vst(sh.units_issued, ++units);
+      next = atomicAdd(&ctl->next_task, 1ull);  // the next unit, claimed ahead
       have_next = true;
+      idle = 0;
       continue;
     }
     if (exhausted && !want_draw && vld(sh.exit_flag)) {
@@ -496,7 +485,7 @@ __device__ __forceinline__ void run_consumers(const VerifyArgs& a, FusedShared& 
 __device__ __forceinline__ void run_arrivals(const VerifyArgs& a, const FusedGeom& g, FusedShared& sh) {
   const int lane = threadIdx.x & 31;
   Partial* partials = static_cast<Partial*>(a.partials);
-  long long u = 0, k3 = 0;
+  long long u = 0;
   bool ok = true;
   unsigned int idle = 0;
   while (true) {
@@ -540,45 +529,16 @@ __device__ __forceinline__ void run_arrivals(const VerifyArgs& a, const FusedGeo
       if (lane == j) mine = Partial{v.x, v.y, v.z, v.w};
     }
     __syncwarp();
-    unsigned int last = 0;
-    int b = 0;
     if (lane < nb) {
       const long long uu = u + lane;
       mbar_arrive(&sh.part_free[uu % kPartBuf]);
-      b = sh.ub[uu % kUQ];
+      const int b = sh.ub[uu % kUQ];
       const long long tau = sh.utau[uu % kUQ];
       partials[tau] = mine;
-      last = (atom_add_acq_rel_gpu(&a.seq[b].arrivals, 1u) + 1u == static_cast<unsigned int>(g.tps)) ? 1u : 0u;
+      red_add_release_gpu(&a.seq[b].arrivals, 1u);  // the Partial is published first
     }
     u += nb;
     if (lane == 0) vst(sh.units_folded, u);
-    unsigned int lm = __ballot_sync(0xffffffffu, last);
-    __syncwarp();  // what the completing lanes acquired is ordered before lane 0's hand-off
-    while (lm) {
-      const int l = __ffs(lm) - 1;
-      lm &= lm - 1;
-      const int bb = __shfl_sync(0xffffffffu, b, l);
-      if (lane == 0) {
-        a.seq[bb].arrivals = 0u;  // the sequence is complete: back to zero
-        const int q = static_cast<int>(k3 % kDQ);
-        if (k3 >= kDQ && !mbar_wait_sleep(&sh.dq_empty[q], static_cast<uint32_t>(((k3 / kDQ) - 1) & 1)))
-          ok = false;
-        sh.dq_b[q] = bb;
-        mbar_arrive(&sh.dq_full[q]);
-        vst(sh.seq_pushed, k3 + 1);
-      }
-      ++k3;
-    }
-    if (!__all_sync(0xffffffffu, ok)) break;
-  }
-  // end marker for the decision warp
-  if (lane == 0) {
-    const int q = static_cast<int>(k3 % kDQ);
-    if (k3 >= kDQ && !mbar_wait_sleep(&sh.dq_empty[q], static_cast<uint32_t>(((k3 / kDQ) - 1) & 1)))
-      ok = false;
-    sh.dq_b[q] = -1;
-    mbar_arrive(&sh.dq_full[q]);
-    vst(sh.seq_pushed, k3 + 1);
   }
   if (!__all_sync(0xffffffffu, ok) && lane == 0) set_abort(sh, a);
 }
@@ -798,16 +758,18 @@ __device__ __noinline__ bool finish_draw(const VerifyArgs& a, const FusedGeom& g
   return false;
 }
 
-// Decision warp: decides the sequences this CTA completed, requests their
-// draws and finishes them.
+// Decision warp: waits for each of this CTA's sequences (b = blockIdx.x,
+// blockIdx.x + gridDim.x, ...) to be counted complete, decides it, requests
+// its draw and finishes the draws in order.
 template <typename E>
 __device__ __forceinline__ void run_decisions(const VerifyArgs& a, const FusedGeom& g, FusedShared& sh,
                                               const unsigned long long* tables, Partial* scratch) {
   const int lane = threadIdx.x & 31;
-  long long k3 = 0, posted = 0, finished = 0;
-  bool end_seen = false, ok = true;
+  long long posted = 0, finished = 0;
+  int nb = blockIdx.x;  // the next sequence this CTA owns
+  bool ok = true;
   unsigned int idle = 0;
-  while (!(end_seen && finished == posted)) {
+  while (nb < g.B || finished < posted) {
     if (vld(sh.abort_flag)) break;
     // the oldest outstanding draw is reduced: finish it (frees its table)
     int r2 = 0;
@@ -836,51 +798,33 @@ __device__ __forceinline__ void run_decisions(const VerifyArgs& a, const FusedGe
       idle = 0;
       continue;
     }
-    // a completed sequence: decide it and request its draw
-    int r3 = 0, b = 0;
-    if (lane == 0 && mbar_test(&sh.dq_full[k3 % kDQ], static_cast<uint32_t>((k3 / kDQ) & 1))) {
-      r3 = 1;
-      b = sh.dq_b[k3 % kDQ];
-      mbar_arrive(&sh.dq_empty[k3 % kDQ]);
-    }
+    // the next owned sequence complete: decide it and request its draw
+    int r3 = 0;
+    if (nb < g.B && lane == 0)
+      r3 = ld_acquire_gpu(&a.seq[nb].arrivals) == static_cast<unsigned int>(g.tps) ? 1 : 0;
     if (__shfl_sync(0xffffffffu, r3, 0)) {
-      b = __shfl_sync(0xffffffffu, b, 0);
-      ++k3;
-      if (b < 0) {
-        end_seen = true;
-      } else {
-        const Job j = decide<E>(a, g, b, scratch, lane);
-        if (posted - finished >= kReq) {  // cannot happen (see kReq)
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          sh.jobs[posted % kReq] = j;
-          __threadfence_block();
-          vst(sh.req_posted, posted + 1);
-        }
-        ++posted;
-      }
-      if (lane == 0) vst(sh.seq_taken, k3);
-      idle = 0;
-      continue;
-    }
-    if (finished == posted) {
-      // nothing in flight: sleep in the barrier until a sequence is handed on
-      int got = 0;
-      if (lane == 0)
-        got = mbar_wait_sleep(&sh.dq_full[k3 % kDQ], static_cast<uint32_t>((k3 / kDQ) & 1)) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, got, 0)) {
+      __syncwarp();  // lane 0's acquire orders every lane's reads of the partials
+      if (lane == 0) a.seq[nb].arrivals = 0u;  // complete: back to zero
+      const Job j = decide<E>(a, g, nb, scratch, lane);
+      if (posted - finished >= kReq) {  // cannot happen: at most one request per owned sequence
         ok = false;
         break;
       }
+      if (lane == 0) {
+        sh.jobs[posted % kReq] = j;
+        __threadfence_block();
+        vst(sh.req_posted, posted + 1);
+      }
+      ++posted;
+      nb += gridDim.x;
+      idle = 0;
       continue;
     }
     if (++idle > kMaxIdle) {
       ok = false;
       break;
     }
-    __nanosleep(256);
+    __nanosleep(finished < posted ? 128 : 512);
   }
   if (lane == 0) vst(sh.exit_flag, 1);
   if (!ok && lane == 0) set_abort(sh, a);
@@ -906,17 +850,11 @@ fused_sample_kernel(VerifyArgs a, FusedGeom g, FusedCtl* ctl) {
     }
     mbar_init(&sh.drawn[0], kCW);
     mbar_init(&sh.drawn[1], kCW);
-    for (int q = 0; q < kDQ; ++q) {
-      mbar_init(&sh.dq_full[q], 1);
-      mbar_init(&sh.dq_empty[q], 1);
-    }
     sh.units_issued = 0;
     sh.units_final = -1;
     sh.units_folded = 0;
     sh.req_posted = 0;
     sh.draws_finished = 0;
-    sh.seq_pushed = 0;
-    sh.seq_taken = 0;
     sh.exit_flag = 0;
     sh.abort_flag = 0;
     fence_barrier_init();
@@ -961,11 +899,20 @@ cudaError_t launch_sample_fused(const VerifyArgs& a, const DeviceInfo& dev, cuda
   long long G = dev.sm_count > 0 ? dev.sm_count : 1;
   if (G > g.total) G = g.total;
   FusedCtl* ctl = static_cast<FusedCtl*>(a.ctl);
-  if (a.bf16)
-    fused_sample_kernel<BF16><<<static_cast<unsigned int>(G), kThreadsF, kSmemF, stream>>>(a, g, ctl);
-  else
-    fused_sample_kernel<F32><<<static_cast<unsigned int>(G), kThreadsF, kSmemF, stream>>>(a, g, ctl);
-  return cudaGetLastError();
+  // cooperative: every CTA is resident, since decision warps wait on the
+  // unit counts that other CTAs' arrival warps publish
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned int>(G));
+  cfg.blockDim = dim3(kThreadsF);
+  cfg.dynamicSmemBytes = kSmemF;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.bf16 ? cudaLaunchKernelEx(&cfg, fused_sample_kernel<BF16>, a, g, ctl)
+                : cudaLaunchKernelEx(&cfg, fused_sample_kernel<F32>, a, g, ctl);
 }
 
 }  // namespace specv
