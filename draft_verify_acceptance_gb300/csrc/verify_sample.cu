@@ -403,7 +403,8 @@ cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream
     const long long nvec = static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16;
     // a draw that fits one segment: the fused kernel draws as it streams;
     // longer rows: the two-kernel sampler, whose per-sequence clusters finish
-    // the last draws sooner
+    // the last draws sooner (measured: the fused kernel takes 59 / 106 us on
+    // the 128256-row bf16 and 152064-row fp32 batches, against 47 / 65)
     if (nvec <= kFusedSeg) return launch_sample_fused(a, dev, stream);
     const int C = sample_2p_cluster(nvec);
     if (C > 0) return launch_sample_2p(a, dev, C, stream);
