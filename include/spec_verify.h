@@ -85,7 +85,7 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 /*
  * Bytes of workspace a call with these sizes needs (a multiple of 256).
  * The workspace holds per-sequence arrival counters, per-row candidates or
- * per-work-unit softmax partials (one unit is a segment of 2048 16-byte
+ * per-work-unit softmax partials (one unit is a segment of 4096 16-byte
  * vectors of a target row and its draft row), and two work counters; its
  * size grows with B, K and V * element size.  It MUST be zero-filled before its first use; every
  * call that returns SPEC_OK leaves it zero-filled again when the kernel
