@@ -185,25 +185,27 @@ greedy_kernel(VerifyArgs a, int nvec, int S, DivU64 by_S, DivU64 by_K1, bool one
     }
   }
 
-  // block argmax on packed keys (larger value, then lower index, wins):
-  // warp butterfly, then the kWarps warp keys butterflied by warp 0
-  unsigned long long key = pack_key(best, bidx);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-    key = o > key ? o : key;
-  }
-  __shared__ unsigned long long s_key[kWarps];
+  // block argmax (larger value, then lower index, wins): per warp, the
+  // largest orderable value and then the lowest index holding it, two
+  // redux.sync each; then the same over the kWarps warp results in warp 0
   const int warp = tid >> 5, lane = tid & 31;
-  if (lane == 0) s_key[warp] = key;
+  unsigned int ov = orderable(best);
+  unsigned int oi = static_cast<unsigned int>(bidx);
+  unsigned int m = __reduce_max_sync(0xffffffffu, ov);
+  oi = __reduce_min_sync(0xffffffffu, ov == m ? oi : 0xffffffffu);
+  __shared__ unsigned int s_v[kWarps], s_i[kWarps];
+  if (lane == 0) {
+    s_v[warp] = m;
+    s_i[warp] = oi;
+  }
   const int any_bad = __syncthreads_or(bad);
   if (warp != 0) return;
-  key = s_key[lane & (kWarps - 1)];
-#pragma unroll
-  for (int off = kWarps / 2; off > 0; off >>= 1) {
-    const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-    key = o > key ? o : key;
-  }
+  ov = lane < kWarps ? s_v[lane] : 0u;
+  oi = lane < kWarps ? s_i[lane] : 0xffffffffu;
+  m = __reduce_max_sync(0xffffffffu, ov);
+  oi = __reduce_min_sync(0xffffffffu, ov == m ? oi : 0xffffffffu);
+  const unsigned long long key =
+      (static_cast<unsigned long long>(m) << 32) | (0xffffffffu - oi);  // as pack_key
   const int b = static_cast<int>(by_K1(row));
 
   if (one_word) {  // one CTA per row: g_i to its slot, one atomic on the sequence
