@@ -144,10 +144,11 @@ greedy_kernel(VerifyArgs a, int nvec, int S, DivU64 by_S, DivU64 by_K1, bool one
                      static_cast<size_t>(row) * static_cast<size_t>(a.V) * E::kBytes;
 
   const int tid = threadIdx.x;
+  const int b = static_cast<int>(by_K1(row));  // sequence, before the stream
   // the draft token this row is compared with, fetched while the row streams
   int xtok = 0;
   if (one_word && tid == 0) {
-    const int b = static_cast<int>(by_K1(row)), pos = row - b * K1;
+    const int pos = row - b * K1;
     if (pos < a.K) xtok = a.tokens[static_cast<size_t>(b) * a.K + pos];
   }
 
@@ -206,7 +207,6 @@ greedy_kernel(VerifyArgs a, int nvec, int S, DivU64 by_S, DivU64 by_K1, bool one
   oi = __reduce_min_sync(0xffffffffu, ov == m ? oi : 0xffffffffu);
   const unsigned long long key =
       (static_cast<unsigned long long>(m) << 32) | (0xffffffffu - oi);  // as pack_key
-  const int b = static_cast<int>(by_K1(row));
 
   if (one_word) {  // one CTA per row: g_i to its slot, one atomic on the sequence
     if (lane == 0) {

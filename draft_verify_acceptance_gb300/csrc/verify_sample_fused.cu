@@ -824,7 +824,7 @@ __device__ __forceinline__ void run_decisions(const VerifyArgs& a, const FusedGe
       ok = false;
       break;
     }
-    __nanosleep(finished < posted ? 128 : 512);
+    __nanosleep(128);
   }
   if (lane == 0) vst(sh.exit_flag, 1);
   if (!ok && lane == 0) set_abort(sh, a);
