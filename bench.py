@@ -215,11 +215,13 @@ def committed_traffic(workload, kernel):
 # --------------------------------------------------------------------------
 # native arm
 # --------------------------------------------------------------------------
-def device_time(binding, inp, steps, warmup, dev, l2_bytes):
+def device_time(binding, inp, steps, warmup, dev, l2_bytes, mode=None):
     """Prepare `steps` launches that rotate over R device copies of the inputs
     (R * bytes > 2x L2), warm up, and capture them in CUDA graphs.  Returns
-    (R, algorithmic bytes per launch, stream, graphs to replay, two events)."""
+    (R, algorithmic bytes per launch, stream, graphs to replay, two events,
+    the output tensors).  `mode` overrides the inputs' mode (early exit)."""
     import torch
+    mode = inp.mode if mode is None else mode
     nbytes = inp.algorithmic_bytes()
     R = max(2, math.ceil(2 * l2_bytes / max(nbytes, 1)) + 1)
     R = min(R, 64)
@@ -236,7 +238,7 @@ def device_time(binding, inp, steps, warmup, dev, l2_bytes):
 
     def launch(r):
         c = copies[r % R]
-        binding.verify(c[0], c[1], c[2], c[3], inp.temperature, inp.mode, stream=stream,
+        binding.verify(c[0], c[1], c[2], c[3], inp.temperature, mode, stream=stream,
                        workspace=ws, out=(acc, out))
 
     with torch.cuda.stream(stream):
@@ -381,7 +383,35 @@ def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
                        "algorithmic_bytes": nbytes}
         del plan
         torch.cuda.empty_cache()
+        if inp.mode == W.MODE_SAMPLE and inp.K > 0:
+            table[name + "+early_exit"] = early_exit_line(binding, inp, steps, dev, l2, peak, sec)
     return table
+
+
+def early_exit_line(binding, inp, steps, dev, l2, peak, parallel_sec):
+    """The same workload in early-exit mode (position 0 first).  Bytes read:
+    position 0's row pairs, plus every row when some sequence accepted x_0
+    (then the full verify runs too); the outputs equal sampling mode's."""
+    import torch
+    R, nbytes, stream, plan, e0, e1, (acc, _) = device_time(
+        binding, inp, steps, 5, dev, l2, mode=binding.MODE_SAMPLE_EARLY_EXIT)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for g in plan:
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = e0.elapsed_time(e1) / 1e3 / steps
+    s = inp.target.element_size()
+    first = 2 * inp.B * inp.V * s + inp.B * 4 + inp.B * 4 + inp.B * (inp.K + 2) * 4
+    full_ran = bool((acc > 0).any().item())  # the last replayed call's outputs
+    read = first + (nbytes if full_ran else 0)
+    del plan
+    torch.cuda.empty_cache()
+    return {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec,
+            "bytes_read": read, "GB_per_s": read / sec / 1e9, "frac_hbm": read / sec / 1e9 / peak,
+            "full_verify_ran": full_ran, "speedup_vs_sampling_mode": parallel_sec / sec}
 
 
 def cpu_baseline(inp, budget_s=10.0):

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 
 MODE_SAMPLE = 0
 MODE_GREEDY = 1
+MODE_SAMPLE_EARLY_EXIT = 2
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
 MAX_K = 64
@@ -114,7 +115,8 @@ def _check(t, name, dtypes, shape, device):
 
 def _mode(mode):
     if isinstance(mode, str):
-        return {"sample": MODE_SAMPLE, "greedy": MODE_GREEDY}[mode]
+        return {"sample": MODE_SAMPLE, "greedy": MODE_GREEDY,
+                "sample_early_exit": MODE_SAMPLE_EARLY_EXIT}[mode]
     return int(mode)
 
 
@@ -128,7 +130,7 @@ def _call(target, draft, tokens, uniforms, temperature, mode, debug, stream, wor
     K = K1 - 1
     _check(target, "target", (torch.float32, torch.bfloat16), (B, K1, V), device)
     dt = DTYPE_BF16 if target.dtype == torch.bfloat16 else DTYPE_F32
-    sample = mode == MODE_SAMPLE
+    sample = mode != MODE_GREEDY
     if K > 0:
         _check(tokens, "tokens", (torch.int32,), (B, K), device)
     if sample:

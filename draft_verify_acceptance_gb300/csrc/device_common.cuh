@@ -69,6 +69,8 @@ inline long long fused_tasks_per_seq(long long K, long long nvec) {
 struct __align__(16) FusedCtl {
   unsigned long long next_task;  // next work unit to hand out
   unsigned long long done_ctas;  // CTAs that have taken their last unit
+  unsigned int pending;          // early exit: sequences that accepted x_0
+  unsigned int pad[3];
 };
 
 // Most ranges the two-kernel sampler's streaming pass cuts the rows into.

@@ -31,6 +31,7 @@ struct VerifyArgs {
   void* partials;              // workspace: Partial per work unit (fused sampler); same
                                // region as `slots`
   void* ctl;                   // workspace: FusedCtl (work counters)
+  bool early_exit = false;     // sampling: verify position 0 first (SPEC_MODE_SAMPLE_EARLY_EXIT)
 };
 
 // Per-device facts gathered once.
@@ -65,5 +66,9 @@ int sample_2p_cluster(long long nvec);
 cudaError_t sample_2p_prepare(DeviceInfo* d);
 cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
                              cudaStream_t stream);
+// Early-exit schedule (aligned rows, K >= 1): position 0 of every sequence,
+// then -- only if some sequence accepted x_0 -- the full two-kernel sampler.
+cudaError_t launch_sample_early_exit(const VerifyArgs& a, const DeviceInfo& dev, int C,
+                                     cudaStream_t stream);
 
 }  // namespace specv

@@ -51,7 +51,8 @@ extern "C" {
 size_t spec_verify_workspace_size(int B, int K, int V, int dtype, int mode) {
   if (B < 0 || K < 0 || K > SPEC_MAX_K || V < 1 || V > SPEC_MAX_V) return 0;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return 0;
-  if (mode != SPEC_MODE_SAMPLE && mode != SPEC_MODE_GREEDY) return 0;
+  if (mode != SPEC_MODE_SAMPLE && mode != SPEC_MODE_GREEDY && mode != SPEC_MODE_SAMPLE_EARLY_EXIT)
+    return 0;
   return specv::workspace_bytes(B, K, V, dtype == SPEC_DTYPE_BF16 ? 2 : 4);
 }
 
@@ -65,9 +66,10 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   // ---- sizes, enums ------------------------------------------------------
   if (B < 0 || K < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
-  if (mode != SPEC_MODE_SAMPLE && mode != SPEC_MODE_GREEDY) return SPEC_ERR_INVALID_ARG;
+  if (mode != SPEC_MODE_SAMPLE && mode != SPEC_MODE_GREEDY && mode != SPEC_MODE_SAMPLE_EARLY_EXIT)
+    return SPEC_ERR_INVALID_ARG;
   if (K > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
-  const bool sample = mode == SPEC_MODE_SAMPLE;
+  const bool sample = mode != SPEC_MODE_GREEDY;
   if (sample && !(temperature > 0.f && std::isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
   if (B == 0) return SPEC_OK;
 
@@ -116,6 +118,7 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   a.slots = static_cast<char*>(workspace) + lay.units;
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
+  a.early_exit = mode == SPEC_MODE_SAMPLE_EARLY_EXIT;
 
   const long long rows = static_cast<long long>(B) * (K + 1);
   if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;

@@ -51,7 +51,7 @@ bool args_ok(const void* target, const void* draft, const int32_t* tokens, const
              int K, int dtype, float temperature, int mode, const int32_t* acc,
              const int32_t* out) {
   const uintptr_t esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
-  const bool sample = mode == SPEC_MODE_SAMPLE;
+  const bool sample = mode != SPEC_MODE_GREEDY;
   if (!target || !aligned(target, esz)) return false;
   if (K > 0 && (!tokens || !aligned(tokens, 4))) return false;
   if (!acc || !aligned(acc, 4) || !out || !aligned(out, 4)) return false;

@@ -405,8 +405,9 @@ cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream
     // longer rows: the two-kernel sampler, whose per-sequence clusters finish
     // the last draws sooner (measured: the fused kernel takes 59 / 106 us on
     // the 128256-row bf16 and 152064-row fp32 batches, against 47 / 65)
-    if (nvec <= kFusedSeg) return launch_sample_fused(a, dev, stream);
     const int C = sample_2p_cluster(nvec);
+    if (a.early_exit && a.K >= 1 && C > 0) return launch_sample_early_exit(a, dev, C, stream);
+    if (nvec <= kFusedSeg) return launch_sample_fused(a, dev, stream);
     if (C > 0) return launch_sample_2p(a, dev, C, stream);
     if (nvec <= kFusedMaxVec) return launch_sample_fused(a, dev, stream);
   }

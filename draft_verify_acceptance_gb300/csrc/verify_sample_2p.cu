@@ -53,6 +53,11 @@ namespace specv {
 struct StreamPartition {
   long long nvec, P, Q, W;
   int G;
+  // 0: a whole verify; 1: early exit, position 0 only (a sequence that
+  // accepts x_0 is counted in *pending and left to phase 2); 2: early exit,
+  // the whole verify, skipped when *pending is 0
+  int phase = 0;
+  unsigned int* pending = nullptr;
   // launch-time constants of the division-free index arithmetic: W = qw*G + rw
   long long qw;
   int rw;
@@ -180,6 +185,8 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
   __shared__ long long s_slot[kMaxPending2];  // partial slot (range + pair) of each parked entry
   __shared__ float4 s_pend[kMaxPending2 * kWarps];
 
+  // early exit: nothing left to verify after position 0
+  if (pt.phase == 2 && *static_cast<volatile unsigned int*>(pt.pending) == 0u) return;
   // the decide-and-sample kernel may be scheduled as soon as SMs free up;
   // it waits for this grid's results before reading them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -334,9 +341,13 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   const int lgC = __ffs(C) - 1;  // C is a power of two
   const int b = static_cast<int>(blockIdx.x >> lgC);
   const int K = a.K, K1 = K + 1;
+  const int Klast = pt.phase == 1 ? 0 : K;  // the last position merged and tested
   const long long nvec = pt.nvec;
   const float s = a.scale;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // early exit: nothing left to verify after position 0 (the whole cluster
+  // reads the same word)
+  if (pt.phase == 2 && *static_cast<volatile unsigned int*>(pt.pending) == 0u) return;
 
   extern __shared__ __align__(16) unsigned long long tws[];  // [tiles][warps] slice masses
   __shared__ Decision s_dec;                           // this CTA's decision
@@ -353,7 +364,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   float2 g0 = make_float2(0.f, 0.f);
   int x0 = 0;
   float u0 = 0.f;
-  if (warp == 0 && lane <= K) {
+  if (warp == 0 && lane <= Klast) {
     u0 = u[lane];
     if (lane < K) {
       x0 = a.tokens[static_cast<size_t>(b) * K + lane];
@@ -368,7 +379,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   // Warp w merges positions w, w + kWB, ...: one lane per contributing range
   // (the loads of up to four positions in flight at once), then a butterfly.
   const Partial* partials = static_cast<const Partial*>(a.partials);
-  for (int i0 = warp; i0 <= K; i0 += 4 * kWB) {
+  for (int i0 = warp; i0 <= Klast; i0 += 4 * kWB) {
     Partial q[4];
     int f[4], l[4];
     long long pp[4];
@@ -379,7 +390,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
       f[t] = 0;
       l[t] = -1;
       pp[t] = 0;
-      if (i <= K) {
+      if (i <= Klast) {
         pp[t] = static_cast<long long>(i) * a.B + b;
         f[t] = pt.cta_of(pp[t] * nvec);
         l[t] = pt.cta_of((pp[t] + 1) * nvec - 1);
@@ -389,7 +400,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int i = i0 + t * kWB;
-      if (i <= K) {  // warp-uniform
+      if (i <= Klast) {  // warp-uniform
         float mt = q[t].ms_t, zt = q[t].z_t, md = q[t].ms_d, zd = q[t].z_d;
         warp_merge_scaled(mt, zt);
         warp_merge_scaled(md, zd);
@@ -414,11 +425,11 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
     const bool writer = rank == 0;
     int n = K, bad = 0, ratio_near = 0;
     float nMSt = 0.f, nZt = 0.f, nMSd = 0.f, nZd = 0.f;
-    for (int i0 = 0; i0 < K1; i0 += 32) {
+    for (int i0 = 0; i0 <= Klast; i0 += 32) {
       const int i = i0 + lane;
       float MSt = -INFINITY, Zt = 0.f, MSd = -INFINITY, Zd = 0.f;
       bool rej = false, nr = false;
-      if (i <= K) {
+      if (i <= Klast) {
         const float4 nz = s_norm[i];
         MSt = nz.x; Zt = nz.y; MSd = nz.z; Zd = nz.w;
         float2 g = g0;
@@ -454,7 +465,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
           ratio_near |= (nb & (pick == 31 ? 0xffffffffu : ((2u << pick) - 1u))) != 0u;
         } else {
           ratio_near |= nb != 0u;
-          if (K - i0 < 32) pick = K - i0;  // the bonus row is in this round
+          if (Klast == K && K - i0 < 32) pick = K - i0;  // the bonus row is in this round
         }
         if (pick >= 0) {
           nMSt = __shfl_sync(0xffffffffu, MSt, pick);
@@ -477,6 +488,21 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
     }
   }
   __syncthreads();
+
+  if (pt.phase == 1 && s_dec.n == K) {
+    // x_0 accepted: this sequence waits for phase 2.  Every CTA of the
+    // cluster has read the partials once all have passed the barrier.
+    cluster_wait();
+    cluster.sync();
+    if (rank == 0 && warp == 0) {
+      Partial* parts = static_cast<Partial*>(a.partials);
+      const long long p = b;  // pair (0, b)
+      const int f = pt.cta_of(p * nvec), l = pt.cta_of((p + 1) * nvec - 1);
+      for (int c = f + lane; c <= l; c += 32) parts[c + p] = Partial{0.f, 0.f, 0.f, 0.f};
+      if (lane == 0) atomicAdd(pt.pending, 1u);
+    }
+    return;
+  }
 
   // ---- this CTA's slice of row pair n (or of the bonus row) -------------
   // read straight from global memory (the rows were streamed moments ago;
@@ -552,7 +578,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   // workspace zero-filled between calls
   if (rank == 0 && warp == 0) {
     Partial* partials = static_cast<Partial*>(a.partials);
-    for (int i = lane; i <= K; i += 32) {
+    for (int i = lane; i <= Klast; i += 32) {
       const long long p = static_cast<long long>(i) * a.B + b;
       const int f = pt.cta_of(p * nvec), l = pt.cta_of((p + 1) * nvec - 1);
       for (int c = f; c <= l; ++c) partials[c + p] = Partial{0.f, 0.f, 0.f, 0.f};
@@ -734,11 +760,13 @@ cudaError_t sample_2p_prepare(DeviceInfo* d) {
   return e;
 }
 
-StreamPartition stream_partition(const VerifyArgs& a, const DeviceInfo& dev) {
+// positions: draft positions streamed (0..positions-1); bonus: the bonus rows too
+StreamPartition stream_partition(const VerifyArgs& a, const DeviceInfo& dev, int positions,
+                                 bool bonus) {
   StreamPartition pt;
   pt.nvec = static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16;
-  pt.P = static_cast<long long>(a.K) * a.B * pt.nvec;
-  pt.Q = static_cast<long long>(a.B) * pt.nvec;
+  pt.P = static_cast<long long>(positions) * a.B * pt.nvec;
+  pt.Q = bonus ? static_cast<long long>(a.B) * pt.nvec : 0;
   pt.W = 2 * pt.P + pt.Q;
   // two CTAs per SM: 8 stages of 16 KiB in flight per SM, and room to compute
   const int per_sm = dev.stream_ctas_per_sm < 2 ? (dev.stream_ctas_per_sm > 0 ? dev.stream_ctas_per_sm : 1) : 2;
@@ -756,9 +784,9 @@ StreamPartition stream_partition(const VerifyArgs& a, const DeviceInfo& dev) {
   return pt;
 }
 
-cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
-                             cudaStream_t stream) {
-  const StreamPartition pt = stream_partition(a, dev);
+// The two kernels over partition pt (the second as a programmatic dependent).
+cudaError_t launch_2p(const VerifyArgs& a, const DeviceInfo& dev, int C, const StreamPartition& pt,
+                      cudaStream_t stream) {
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned int>(pt.G));
@@ -795,6 +823,31 @@ cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
                   : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32, 512>, a, pt);
   return a.bf16 ? cudaLaunchKernelEx(&cfg, decide_sample_kernel<BF16, kThreads>, a, pt)
                 : cudaLaunchKernelEx(&cfg, decide_sample_kernel<F32, kThreads>, a, pt);
+}
+
+cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
+                             cudaStream_t stream) {
+  return launch_2p(a, dev, C, stream_partition(a, dev, a.K, true), stream);
+}
+
+cudaError_t launch_sample_early_exit(const VerifyArgs& a, const DeviceInfo& dev, int C,
+                                     cudaStream_t stream) {
+  unsigned int* pending = &static_cast<FusedCtl*>(a.ctl)->pending;
+  // phase 1: position 0's row pairs; rejecting sequences are drawn and done
+  StreamPartition p1 = stream_partition(a, dev, 1, false);
+  p1.phase = 1;
+  p1.pending = pending;
+  cudaError_t e = launch_2p(a, dev, C, p1, stream);
+  if (e != cudaSuccess) return e;
+  // phase 2: the whole verify, which both kernels skip on the device when
+  // no sequence accepted x_0; it recomputes every sequence, the phase-1 ones
+  // included (same result, up to the flagged boundary cases)
+  StreamPartition p2 = stream_partition(a, dev, a.K, true);
+  p2.phase = 2;
+  p2.pending = pending;
+  e = launch_2p(a, dev, C, p2, stream);
+  if (e != cudaSuccess) return e;
+  return cudaMemsetAsync(pending, 0, sizeof(unsigned int), stream);  // zero at rest
 }
 
 }  // namespace specv

@@ -60,7 +60,11 @@ typedef enum {
                                 SPEC_STATIC_SCRATCH_BYTES */
 } spec_status_t;
 
-typedef enum { SPEC_MODE_SAMPLE = 0, SPEC_MODE_GREEDY = 1 } spec_mode_t;
+typedef enum {
+  SPEC_MODE_SAMPLE = 0,
+  SPEC_MODE_GREEDY = 1,
+  SPEC_MODE_SAMPLE_EARLY_EXIT = 2  /* sampling, position 0 verified first (below) */
+} spec_mode_t;
 typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 
 /* Build limits. */
@@ -114,7 +118,8 @@ SPEC_API size_t spec_verify_workspace_size(int B, int K, int V, int dtype, int m
  *   dtype                      SPEC_DTYPE_F32 or SPEC_DTYPE_BF16 (both logits).
  *   temperature                > 0 and finite in sampling mode: p = softmax(t/T),
  *                              q = softmax(d/T).  Ignored in greedy mode.
- *   mode                       SPEC_MODE_SAMPLE or SPEC_MODE_GREEDY.
+ *   mode                       SPEC_MODE_SAMPLE, SPEC_MODE_GREEDY or
+ *                              SPEC_MODE_SAMPLE_EARLY_EXIT.
  *   accepted_len  [B]          int32 out, device: n = number of accepted draft
  *                              tokens, in [0, K].
  *   out_tokens    [B, K+1]     int32 out, device: x_0..x_{n-1}, then the
@@ -130,6 +135,16 @@ SPEC_API size_t spec_verify_workspace_size(int B, int K, int V, int dtype, int m
  * with C_j > u_K * S, C the inclusive running sum in token order of
  * max(0, p_n - q_n) and S its total (p_n itself if S == 0); at n == K the
  * same inverse CDF is taken on p_K.
+ * Early-exit sampling mode:  the same outputs as sampling mode, from a
+ * schedule that reads position 0's row pair of every sequence first, decides
+ * position 0 and draws the replacement of each sequence that rejects there;
+ * only if some sequence accepts x_0 are all rows read and every sequence
+ * verified as in sampling mode.  When most sequences reject their first
+ * draft token (a poor drafter) this reads 2/(2K+1) of the rows; otherwise it
+ * costs one extra pass over position 0.  16-byte aligned rows with K >= 1
+ * only; other calls run as sampling mode.  When no sequence accepts x_0,
+ * p_at_draft / q_at_draft (see spec_verify_ex) are written for position 0
+ * only and device_status covers only the rows read.
  * Greedy mode:  g_i = argmax_j t[b, i, j] compared as fp32 values, lowest index
  * on ties; n = first i < K with x_i != g_i (K if none); the emitted token at n
  * is g_n.

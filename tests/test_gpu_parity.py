@@ -42,6 +42,13 @@ def run_gpu(lib, inp, **kw):
     return {k: v.cpu().numpy() for k, v in res.items()}
 
 
+def run_gpu_mode(lib, inp, mode):
+    res = lib.verify_ex(_dev(inp.target), _dev(inp.draft), _dev(inp.tokens), _dev(inp.uniforms),
+                        inp.temperature, mode)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
 def run_oracle(inp):
     return oracle.verify_ref(W.as_numpy_logits(inp.target), W.as_numpy_logits(inp.draft),
                              inp.tokens.numpy(),
@@ -137,6 +144,61 @@ def test_greedy_parity(lib, name, B, K, V, dtype, recipe):
     inp = W.make_inputs(B, K, V, dtype=dtype, mode=W.MODE_GREEDY, seed=zlib.crc32(name.encode()) % 1000,
                         name=name, **recipe)
     assert_parity(run_gpu(lib, inp), run_oracle(inp), inp, name)
+
+
+EARLY_EXIT_CASES = [
+    # (name, B, K, V, dtype, T, recipe): low acceptance (phase 2 usually
+    # skipped), moderate and high acceptance (phase 2 runs), K = 1, short rows
+    ("ee_f32_independent", 12, 16, 20000, torch.float32, 0.8, dict(target_std=5.0, independent_draft=True)),
+    ("ee_bf16_noise", 48, 5, 40000, torch.bfloat16, 1.0, dict(target_std=4.0, zipf_s=1.1, draft_noise=1.0)),
+    ("ee_bf16_close", 16, 4, 32000, torch.bfloat16, 1.0, dict(target_std=3.0, draft_noise=0.3)),
+    ("ee_f32_K1", 20, 1, 5000, torch.float32, 0.7, dict(target_std=3.0, draft_noise=2.0)),
+    ("ee_f32_short", 6, 3, 1000, torch.float32, 1.0, dict(target_std=3.0, independent_draft=True)),
+]
+
+
+def assert_parity_early_exit(g, ref, inp, label):
+    """Outputs as in sampling mode; diagnostics for position 0 always, for
+    every position when some sequence accepted x_0 (the full pass ran)."""
+    assert int(g["status"][0]) == ref["status"] == 0, label
+    check_valid(g, inp)
+    flagged = ref["flags"] != 0
+    bad = (g["accepted_len"] != ref["accepted_len"]) | (g["out_tokens"] != ref["out_tokens"]).any(1)
+    assert not (bad & ~flagged).any(), (label, np.nonzero(bad & ~flagged)[0][:5])
+    tol = 1e-5 if inp.target.dtype == torch.float32 else 2e-3
+    cols = slice(None) if (g["accepted_len"] > 0).any() else slice(0, 1)
+    assert np.abs(g["p_at"][:, cols] - ref["p_at"][:, cols]).max() <= tol, label
+    assert np.abs(g["q_at"][:, cols] - ref["q_at"][:, cols]).max() <= tol, label
+
+
+@pytest.mark.parametrize("name,B,K,V,dtype,T,recipe", EARLY_EXIT_CASES, ids=[c[0] for c in EARLY_EXIT_CASES])
+def test_early_exit_parity(lib, name, B, K, V, dtype, T, recipe):
+    inp = W.make_inputs(B, K, V, dtype=dtype, temperature=T, seed=zlib.crc32(name.encode()) % 1000,
+                        name=name, **recipe)
+    g = run_gpu_mode(lib, inp, "sample_early_exit")
+    assert_parity_early_exit(g, run_oracle(inp), inp, name)
+
+
+def test_early_exit_full_size_long_draft(lib):
+    """The fp32 long-draft batch: every sequence rejects its first draft token."""
+    inp = W.workload("long_draft_f32_B16_K16_V152064_T0.8")
+    g = run_gpu_mode(lib, inp, "sample_early_exit")
+    ref = run_oracle(inp)
+    assert (ref["accepted_len"] == 0).all()
+    assert_parity_early_exit(g, ref, inp, inp.name)
+
+
+def test_early_exit_workspace_left_zero(lib):
+    for name, B, K, V, dtype, T, recipe in EARLY_EXIT_CASES[:3]:
+        inp = W.make_inputs(B, K, V, dtype=dtype, temperature=T, seed=7, name=name, **recipe)
+        dt = lib.DTYPE_BF16 if dtype == torch.bfloat16 else lib.DTYPE_F32
+        ws = torch.zeros(lib.workspace_size(B, K, V, dt, lib.MODE_SAMPLE_EARLY_EXIT),
+                         dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            lib.verify(_dev(inp.target), _dev(inp.draft), _dev(inp.tokens), _dev(inp.uniforms),
+                       T, "sample_early_exit", workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero().item()) == 0, name
 
 
 def test_greedy_ties_take_the_lowest_index(lib):

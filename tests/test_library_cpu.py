@@ -61,6 +61,7 @@ def test_header_constants_match_binding(binding):
     assert d["SPEC_STATIC_SCRATCH_BYTES"] == binding.STATIC_SCRATCH_BYTES
     assert d["SPEC_MODE_SAMPLE"] == binding.MODE_SAMPLE
     assert d["SPEC_MODE_GREEDY"] == binding.MODE_GREEDY
+    assert d["SPEC_MODE_SAMPLE_EARLY_EXIT"] == binding.MODE_SAMPLE_EARLY_EXIT
     assert d["SPEC_DTYPE_F32"] == binding.DTYPE_F32
     assert d["SPEC_DTYPE_BF16"] == binding.DTYPE_BF16
     assert d["SPEC_MAX_K"] == binding.MAX_K
@@ -90,7 +91,8 @@ def test_workspace_size(binding):
     assert ws(4, 65, 10, 0, 0) == 0
     assert ws(4, 4, 0, 0, 0) == 0
     assert ws(4, 4, 10, 2, 0) == 0
-    assert ws(4, 4, 10, 0, 2) == 0
+    assert ws(4, 4, 10, 0, 3) == 0
+    assert ws(4, 4, 10, 0, binding.MODE_SAMPLE_EARLY_EXIT) == ws(4, 4, 10, 0, binding.MODE_SAMPLE)
     assert ws(4, 4, binding.MAX_V + 1, 0, 0) == 0
 
 
