@@ -70,7 +70,7 @@ struct __align__(16) FusedCtl {
   unsigned long long next_task;  // next work unit to hand out
   unsigned long long done_ctas;  // CTAs that have taken their last unit
   unsigned int pending;          // early exit: sequences that accepted x_0
-  unsigned int pad[3];
+  unsigned int pad[3];           // pad[0]: early exit, phase-2 CTAs finished
 };
 
 // Most ranges the two-kernel sampler's streaming pass cuts the rows into.

@@ -692,6 +692,15 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
       if (a.flags) a.flags[b] = (dec.ratio_near ? kFlagRatio : 0u) | (near ? kFlagCdf : 0u);
     }
   }
+  // early exit, phase 2 (it ran, so *pending > 0): the last CTA to finish --
+  // every CTA of the grid has read *pending by then -- puts it back to zero
+  if (pt.phase == 2 && tid == 0) {
+    FusedCtl* ctl = static_cast<FusedCtl*>(a.ctl);
+    if (atom_add_acq_rel_gpu(&ctl->pad[0], 1u) + 1u == gridDim.x) {
+      ctl->pending = 0u;
+      ctl->pad[0] = 0u;
+    }
+  }
 }
 
 size_t smem_b(long long nvec, int C, int nt) {
@@ -845,9 +854,9 @@ cudaError_t launch_sample_early_exit(const VerifyArgs& a, const DeviceInfo& dev,
   StreamPartition p2 = stream_partition(a, dev, a.K, true);
   p2.phase = 2;
   p2.pending = pending;
-  e = launch_2p(a, dev, C, p2, stream);
-  if (e != cudaSuccess) return e;
-  return cudaMemsetAsync(pending, 0, sizeof(unsigned int), stream);  // zero at rest
+  // (*pending is zero at rest again: untouched when phase 2 is skipped,
+  // reset by phase 2's last CTA otherwise)
+  return launch_2p(a, dev, C, p2, stream);
 }
 
 }  // namespace specv
