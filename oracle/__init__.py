@@ -42,6 +42,9 @@ def _load():
         lib.spec_oracle_verify.argtypes = [
             P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P]
+        lib.spec_oracle_draft_sample.restype = ctypes.c_int
+        lib.spec_oracle_draft_sample.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_double, P, P, P, P]
         lib.spec_oracle_softmax.restype = ctypes.c_int
         lib.spec_oracle_softmax.argtypes = [P, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, P]
@@ -101,6 +104,31 @@ def verify_ref(target, draft, tokens, uniforms, temperature=1.0,
     if want_debug:
         res.update(p_at=p_at, q_at=q_at, flags=flags)
     return res
+
+
+def draft_sample_ref(logits, uniforms, temperature=1.0):
+    """The drafter's sampling step: x ~ softmax(row / T) by inverse CDF with
+    one uniform per row.  logits [..., V] (float32 or bf16 bits as uint16),
+    uniforms [...] float32.  Returns tokens (int32), q_at = q(x) (float64),
+    flags (uint32) shaped like the uniforms, and status."""
+    lib = _load()
+    t, dt = _logits(logits, "logits")
+    V = t.shape[-1]
+    R = t.size // V
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(-1)
+    if u.size != R:
+        raise ValueError("one uniform per row")
+    tok = np.empty(R, np.int32)
+    q = np.empty(R, np.float64)
+    flags = np.empty(R, np.uint32)
+    status = ctypes.c_int32(0)
+    rc = lib.spec_oracle_draft_sample(_ptr(t), _ptr(u), R, V, dt, float(temperature), _ptr(tok),
+                                      _ptr(q), _ptr(flags), ctypes.byref(status))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    shape = t.shape[:-1]
+    return {"tokens": tok.reshape(shape), "q_at": q.reshape(shape),
+            "flags": flags.reshape(shape), "status": status.value}
 
 
 def softmax_ref(row, temperature=1.0):

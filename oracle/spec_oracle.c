@@ -328,6 +328,44 @@ int spec_oracle_verify(const void* target, const void* draft, const int32_t* tok
   return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 
+/* The drafter's own sampling step, the one before verification ([SRS]
+ * 技术原理与步骤 step 1, the draft model proposes its tokens; [SCD]
+ * "Speculative Decoding": x_i is sampled from the draft's distribution):
+ * for each of R rows, q = softmax(row / T) and x = the inverse-CDF draw of
+ * q with u[r] (the same rule as the verifier's draws); q_at[r] = q(x).
+ * flags[r] gets ORACLE_FLAG_CDF near a CDF step; a row with NaN / +inf or no
+ * finite entry sets ORACLE_DATA_LOGIT in *status (token 0, q_at 0), a
+ * uniform outside [0, 1) ORACLE_DATA_UNIFORM. */
+int spec_oracle_draft_sample(const void* logits, const float* uniforms, int R, int V, int dtype,
+                             double temperature, int32_t* tokens, double* q_at, uint32_t* flags,
+                             int32_t* status) {
+  if (!logits || !uniforms || !tokens || R < 0 || V < 1 || !(temperature > 0.0))
+    return ORACLE_ERR_INVALID_ARG;
+  int total = 0, nomem = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : total) reduction(| : nomem)
+  for (int r = 0; r < R; ++r) {
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!p) { nomem = 1; continue; }
+    uint32_t fl = 0;
+    int tok = 0;
+    double qx = 0.0;
+    int st = row_softmax(logits, dtype, (size_t)r * (size_t)V, V, temperature, p);
+    const double u = (double)uniforms[r];
+    if (!(u >= 0.0 && u < 1.0)) st |= ORACLE_DATA_UNIFORM;
+    if (!(st & ORACLE_DATA_LOGIT)) {
+      tok = inverse_cdf(p, V, u >= 0.0 && u < 1.0 ? u : 0.0, &fl);
+      qx = p[tok];
+    }
+    tokens[r] = tok;
+    if (q_at) q_at[r] = qx;
+    if (flags) flags[r] = fl;
+    total |= st;
+    free(p);
+  }
+  if (status) *status = total;
+  return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
 /* The temperature softmax of one row, for the tests that pin it against a
  * library softmax.  Returns ORACLE_DATA_LOGIT for a row it refuses. */
 int spec_oracle_softmax(const void* row, int V, int dtype, double temperature, double* p) {

@@ -516,3 +516,58 @@ def test_boundary_flags_mark_uniforms_near_a_threshold():
     d2 = [[0.0, 0.0]]
     r = _one(t2, d2, [0], [0.1, 0.5])
     assert r["flags"][0] & oracle.FLAG_CDF
+
+
+# --------------------------------------------------------------------------
+# the drafter's sampling step (x ~ softmax(d / T) by inverse CDF)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_draft_sample_q_is_the_library_softmax_at_the_token(dtype):
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(6, 300, generator=g) * 3.0
+    x[:, ::7] = float("-inf")
+    u = torch.rand(6, generator=g)
+    if dtype == "bf16":
+        xb = x.to(torch.bfloat16)
+        arr, xd = xb.view(torch.int16).numpy().view(np.uint16), xb.double()
+    else:
+        arr, xd = x.numpy(), x.double()
+    r = oracle.draft_sample_ref(arr, u.numpy(), 0.8)
+    p = torch.softmax(xd / 0.8, dim=-1).numpy()
+    rows = np.arange(6)
+    np.testing.assert_allclose(r["q_at"], p[rows, r["tokens"]], rtol=1e-12, atol=0)
+    assert (p[rows, r["tokens"]] > 0).all()  # never a token without mass
+
+
+def test_draft_sample_inverse_cdf_on_a_uniform_grid():
+    """Uniforms on an even grid land in each token's CDF step in proportion to
+    its probability: N*p_j of the N grid points, within one (plus float32
+    rounding of the grid)."""
+    logits = np.array([0.3, -1.2, 2.0, 0.0, -0.5], np.float32)
+    N = 20000
+    u = ((np.arange(N) + 0.5) / N).astype(np.float32)
+    r = oracle.draft_sample_ref(np.tile(logits, (N, 1)), u, 1.0)
+    p = torch.softmax(torch.tensor(logits, dtype=torch.float64), 0).numpy()
+    counts = np.bincount(r["tokens"], minlength=5)
+    assert np.abs(counts - N * p).max() <= 2.0
+    # and the tokens are nondecreasing in u (an inverse CDF in token order)
+    assert (np.diff(r["tokens"]) >= 0).all()
+
+
+def test_draft_sample_equals_the_verifiers_bonus_draw():
+    """With K = 0 the verifier's only draw is the bonus draw from p_0: the
+    same inverse CDF on the same softmax."""
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn(9, 1000, generator=g) * 4.0).numpy()
+    u = torch.rand(9, generator=g).numpy()
+    r = oracle.draft_sample_ref(x, u, 1.3)
+    v = oracle.verify_ref(x[:, None, :], None, np.zeros((9, 0), np.int32), u[:, None], 1.3)
+    np.testing.assert_array_equal(r["tokens"], v["out_tokens"][:, 0])
+
+
+def test_draft_sample_data_errors():
+    x = np.zeros((3, 10), np.float32)
+    x[1, 4] = np.nan
+    u = np.array([0.5, 0.5, 1.5], np.float32)
+    r = oracle.draft_sample_ref(x, u, 1.0)
+    assert r["status"] == oracle.DATA_LOGIT | oracle.DATA_UNIFORM
