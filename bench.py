@@ -385,7 +385,48 @@ def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
         torch.cuda.empty_cache()
         if inp.mode == W.MODE_SAMPLE and inp.K > 0:
             table[name + "+early_exit"] = early_exit_line(binding, inp, steps, dev, l2, peak, sec)
+            table[name + "+draft_sample"] = draft_sample_line(binding, inp, steps, dev, l2, peak)
     return table
+
+
+def draft_sample_line(binding, inp, steps, dev, l2, peak):
+    """The drafter's sampling step over the workload's B*K draft rows (one
+    uniform each), graph-replayed over rotating copies > 2x L2 like the rest."""
+    import torch
+    s = inp.draft.element_size()
+    nbytes = inp.B * inp.K * inp.V * s + inp.B * inp.K * 4 * 3
+    R = min(64, max(2, math.ceil(2 * l2 / max(nbytes, 1)) + 1))
+    copies = [inp.draft.to(dev) for _ in range(R)]
+    u = inp.uniforms[:, :inp.K].contiguous().to(dev)
+    dt = binding.DTYPE_BF16 if inp.draft.dtype == torch.bfloat16 else binding.DTYPE_F32
+    ws = torch.zeros(binding.workspace_size(inp.B * inp.K, 0, inp.V, dt, binding.MODE_SAMPLE),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    out = (torch.empty(u.shape, dtype=torch.int32, device=dev),
+           torch.empty(u.shape, dtype=torch.float32, device=dev))
+    with torch.cuda.stream(stream):
+        for r in range(3):
+            binding.draft_sample(copies[r % R], u, inp.temperature, stream=stream, workspace=ws,
+                                 out=out)
+        stream.synchronize()
+        n = min(steps, 1000)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n):
+                binding.draft_sample(copies[k % R], u, inp.temperature, stream=stream, workspace=ws,
+                                     out=out)
+        g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    del g, copies
+    torch.cuda.empty_cache()
+    return {"us_per_step": sec * 1e6, "rows_per_s": inp.B * inp.K / sec, "bytes": nbytes,
+            "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak}
 
 
 def early_exit_line(binding, inp, steps, dev, l2, peak, parallel_sec):

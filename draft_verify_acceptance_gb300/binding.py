@@ -38,7 +38,7 @@ FLAG_RATIO = 1
 FLAG_CDF = 2
 
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_status_string",
-           "spec_verify_static")
+           "spec_verify_static", "spec_draft_sample")
 
 
 class SpecVerifyError(RuntimeError):
@@ -62,6 +62,8 @@ def _load():
     lib.spec_verify_ex.argtypes = [P, P, P, P, I, I, I, I, F, I, P, P, P, Z, P, P, P, P, P]
     lib.spec_verify_static.restype = I
     lib.spec_verify_static.argtypes = [P, P, P, P, I, I, I, I, F, I, P, P, P]
+    lib.spec_draft_sample.restype = I
+    lib.spec_draft_sample.argtypes = [P, P, I, I, I, F, P, P, P, Z, P, P]
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [I]
     return lib
@@ -203,6 +205,44 @@ def verify_ex(target, draft=None, tokens=None, uniforms=None, temperature=1.0, m
     acc, out, ex = _call(target, draft, tokens, uniforms, temperature, mode, True, stream, workspace)
     ex.update(accepted_len=acc, out_tokens=out)
     return ex
+
+
+def draft_sample(logits, uniforms, temperature=1.0, *, stream=None, workspace=None, out=None,
+                 debug=False):
+    """The drafter's sampling step on the GPU: for each row of ``logits``
+    ([..., V], float32 or bfloat16, CUDA, 16-byte aligned rows) draw x from
+    softmax(row / T) by inverse CDF with the matching uniform ([...] float32).
+    Returns (tokens int32 [...], q_at float32 [...] = q(x)), plus the status
+    word when ``debug``, queued on ``stream``; ``out`` may give preallocated
+    (tokens, q_at)."""
+    if logits is None or logits.dim() < 1:
+        raise ValueError("logits must be [..., V]")
+    device = logits.device
+    V = logits.shape[-1]
+    R = logits.numel() // V if V else 0
+    _check(logits, "logits", (torch.float32, torch.bfloat16), tuple(logits.shape), device)
+    _check(uniforms, "uniforms", (torch.float32,), tuple(logits.shape[:-1]), device)
+    dt = DTYPE_BF16 if logits.dtype == torch.bfloat16 else DTYPE_F32
+    stream = stream or torch.cuda.current_stream(device)
+    if out is not None:
+        tokens, q_at = out
+        _check(tokens, "tokens", (torch.int32,), tuple(logits.shape[:-1]), device)
+        _check(q_at, "q_at", (torch.float32,), tuple(logits.shape[:-1]), device)
+    else:
+        tokens = torch.empty(logits.shape[:-1], dtype=torch.int32, device=device)
+        q_at = torch.empty(logits.shape[:-1], dtype=torch.float32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device) if debug else None
+    need = workspace_size(R, 0, V, dt, MODE_SAMPLE)
+    if need == 0 and R > 0:
+        raise SpecVerifyError(ERR_UNSUPPORTED if V > MAX_V else ERR_INVALID_ARG, "workspace size")
+    ws = workspace if workspace is not None else workspace_for(device, stream, need)
+    with torch.cuda.device(device):
+        rc = _lib.spec_draft_sample(_ptr(logits), _ptr(uniforms), R, V, dt, float(temperature),
+                                    _ptr(tokens), _ptr(q_at), _ptr(ws), ws.numel(),
+                                    ctypes.c_void_p(stream.cuda_stream), _ptr(status))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_draft_sample")
+    return (tokens, q_at, status) if debug else (tokens, q_at)
 
 
 def _verify_host(target, draft, tokens, uniforms, temperature, mode, stream):

@@ -20,7 +20,7 @@ struct VerifyArgs {
   bool bf16;                   // element type of both logit tensors
   bool vec;                    // rows are 16-byte aligned: 16-byte vector loads
   float scale;                 // log2(e) / T (sampling)
-  int32_t* accepted_len;       // [B]
+  int32_t* accepted_len;       // [B] (null: not written; the draft sampler)
   int32_t* out_tokens;         // [B, K+1]
   float* p_at;                 // [B, K] or null
   float* q_at;                 // [B, K] or null
@@ -32,6 +32,8 @@ struct VerifyArgs {
                                // region as `slots`
   void* ctl;                   // workspace: FusedCtl (work counters)
   bool early_exit = false;     // sampling: verify position 0 first (SPEC_MODE_SAMPLE_EARLY_EXIT)
+  float* p_emit = nullptr;     // [B] or null: p_n of the token emitted at position n
+                               // (fused and two-kernel samplers; the draft sampler's q(x))
 };
 
 // Per-device facts gathered once.

@@ -367,7 +367,7 @@ __device__ __forceinline__ void warp_arrive_and_finalize(const VerifyArgs& a, in
   __syncwarp();
   for (int j = lane; j < K1; j += 32) *candidate_slot(a, b, j) = 0;
   if (lane == 0) {
-    a.accepted_len[b] = n;
+    if (a.accepted_len) a.accepted_len[b] = n;
     if (a.flags) {
       const unsigned long long evaluated = (n >= 63) ? ~0ull : ((2ull << n) - 1ull);
       a.flags[b] = ((near & evaluated) ? kFlagRatio : 0u) | ((c < 0) ? kFlagCdf : 0u);

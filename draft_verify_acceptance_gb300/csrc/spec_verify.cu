@@ -143,6 +143,61 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
                         workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr);
 }
 
+spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R, int V, int dtype,
+                                float temperature, int32_t* tokens, float* q_at, void* workspace,
+                                size_t workspace_bytes, spec_stream_t stream,
+                                int32_t* device_status) {
+  if (R < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
+  if (!(temperature > 0.f && std::isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
+  if (R == 0) return SPEC_OK;
+  const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  if (!logits || !aligned(logits, esz)) return SPEC_ERR_INVALID_ARG;
+  if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_INVALID_ARG;
+  if (!tokens || !aligned(tokens, 4)) return SPEC_ERR_INVALID_ARG;
+  if ((q_at && !aligned(q_at, 4)) || (device_status && !aligned(device_status, 4)))
+    return SPEC_ERR_INVALID_ARG;
+  const size_t need = specv::workspace_bytes(R, 0, V, esz);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return SPEC_ERR_INVALID_ARG;
+  const long long rowbytes = static_cast<long long>(V) * esz;
+  if (rowbytes % 16 != 0 || !aligned(logits, 16)) return SPEC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(R) * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  specv::DeviceInfo info;
+  if (specv::device_info(dev, &info) != cudaSuccess) return SPEC_ERR_CUDA;
+
+  // a verify of R sequences with K = 0: its one draw is the bonus draw from
+  // p_0 = softmax(row / T) with u[r], and p_emit is p_0 at the drawn token
+  specv::VerifyArgs a;
+  a.target = logits;
+  a.draft = nullptr;
+  a.tokens = nullptr;
+  a.uniforms = uniforms;
+  a.B = R;
+  a.K = 0;
+  a.V = V;
+  a.bf16 = dtype == SPEC_DTYPE_BF16;
+  a.vec = true;
+  a.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.accepted_len = nullptr;
+  a.out_tokens = tokens;
+  a.p_at = nullptr;
+  a.q_at = nullptr;
+  a.flags = nullptr;
+  a.status = device_status;
+  a.p_emit = q_at;
+  const specv::WorkspaceLayout lay = specv::workspace_layout(R, 0, V, esz);
+  a.seq = reinterpret_cast<specv::SeqState*>(static_cast<char*>(workspace) + lay.seq);
+  a.slots = static_cast<char*>(workspace) + lay.units;
+  a.partials = static_cast<char*>(workspace) + lay.units;
+  a.ctl = static_cast<char*>(workspace) + lay.ctl;
+  const cudaError_t e = specv::launch_sample(a, info, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
 const char* spec_status_string(int status) {
   switch (status) {
     case SPEC_OK: return "ok";

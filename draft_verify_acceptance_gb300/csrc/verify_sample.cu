@@ -77,7 +77,7 @@ __device__ void finalize_sequence(const VerifyArgs& a, int b) {
   for (int j = 0; j < n; ++j) out[j] = min(max(x[j], 0), a.V - 1);
   out[n] = c & 0x7fffffff;
   for (int j = n + 1; j < K1; ++j) out[j] = -1;
-  a.accepted_len[b] = n;
+  if (a.accepted_len) a.accepted_len[b] = n;
   if (a.flags) {
     const unsigned long long evaluated = (n >= 63) ? ~0ull : ((2ull << n) - 1ull);
     a.flags[b] = ((near & evaluated) ? kFlagRatio : 0u) | ((c < 0) ? kFlagCdf : 0u);

@@ -688,8 +688,12 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
     for (int j = lane; j < K1; j += 32)
       out[j] = (j < n) ? min(max(x[j], 0), a.V - 1) : (j == n ? token : -1);
     if (lane == 0) {
-      a.accepted_len[b] = n;
+      if (a.accepted_len) a.accepted_len[b] = n;
       if (a.flags) a.flags[b] = (dec.ratio_near ? kFlagRatio : 0u) | (near ? kFlagCdf : 0u);
+      if (a.p_emit) {  // p_n(token) from the drawn row's normaliser
+        const float xt = load_one<E>(a.target, (static_cast<long long>(b) * K1 + n) * a.V + token);
+        a.p_emit[b] = ex2(fmaf(xt, s, -dec.MSt)) / dec.Zt;
+      }
     }
   }
   // early exit, phase 2 (it ran, so *pending > 0): the last CTA to finish --

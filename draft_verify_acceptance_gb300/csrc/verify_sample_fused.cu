@@ -752,8 +752,12 @@ __device__ __noinline__ bool finish_draw(const VerifyArgs& a, const FusedGeom& g
   for (int jj = lane; jj < K1; jj += 32)
     out[jj] = (jj < n) ? min(max(x[jj], 0), a.V - 1) : (jj == n ? token : -1);
   if (lane == 0) {
-    a.accepted_len[b] = n;
+    if (a.accepted_len) a.accepted_len[b] = n;
     if (a.flags) a.flags[b] = (j.ratio_near ? kFlagRatio : 0u) | (near ? kFlagCdf : 0u);
+    if (a.p_emit) {  // p_n(token) from the drawn row's normaliser
+      const float xt = load_one<E>(a.target, (static_cast<long long>(b) * K1 + n) * a.V + token);
+      a.p_emit[b] = ex2(fmaf(xt, a.scale, -j.MSt)) * j.invZt;
+    }
   }
   return false;
 }

@@ -212,6 +212,36 @@ SPEC_API spec_status_t spec_verify_static(const void* target_logits, const void*
                                           int mode, int32_t* accepted_len, int32_t* out_tokens,
                                           spec_stream_t stream);
 
+/*
+ * spec_draft_sample -- the drafter's own sampling step, the one before
+ * verification ("推测性拒绝采样", 技术原理与步骤 step 1; "논문 리뷰
+ * [Speculative Contrastive Decoding]", Speculative Decoding: the draft model
+ * samples x_i from its distribution q_i).  For each of R rows:
+ *
+ *   q = softmax(row / T);  x = the smallest token j with C_j > u * S, C the
+ *   inclusive running sum of q in token order and S its total (the same
+ *   inverse CDF, on the same fixed-point scheme, as spec_verify's draws).
+ *
+ *   logits     [R, V]  dtype, device (for example the draft's [B, K, V]
+ *              logits, R = B*K).  Rows must be 16-byte aligned: V times the
+ *              element size a multiple of 16, base 16-byte aligned; other
+ *              rows give SPEC_ERR_UNSUPPORTED.
+ *   uniforms   [R] fp32 in [0, 1), device.
+ *   temperature > 0 and finite.
+ *   tokens     [R] int32 out, device: x.
+ *   q_at       [R] fp32 out, device, or NULL: q(x).
+ *   workspace  as spec_verify's, spec_verify_workspace_size(R, 0, V, dtype,
+ *              SPEC_MODE_SAMPLE) bytes, zero-filled before first use and left
+ *              zero-filled.
+ *   device_status  int32 in/out or NULL: SPEC_DATA_* bits, as spec_verify_ex.
+ *
+ * Asynchronous on `stream`; argument errors return before any launch.
+ */
+SPEC_API spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R, int V,
+                                         int dtype, float temperature, int32_t* tokens,
+                                         float* q_at, void* workspace, size_t workspace_bytes,
+                                         spec_stream_t stream, int32_t* device_status);
+
 /* A short, static, human-readable description of a return code. */
 SPEC_API const char* spec_status_string(int status);
 

@@ -331,3 +331,41 @@ def test_bad_arguments_raise_before_launch(lib):
         lib.verify(t, torch.zeros((2, 2, 10), device="cuda"),
                    torch.zeros((2, 2), dtype=torch.int32, device="cuda"),
                    torch.zeros((2, 3), device="cuda"), 0.0)
+
+
+DRAFT_SAMPLE_CASES = [
+    # (name, rows shape, V, dtype, T): fused-kernel rows, two-kernel rows
+    ("ds_f32_short", (5, 3), 1000, torch.float32, 1.0),
+    ("ds_bf16_32000", (8, 4), 32000, torch.bfloat16, 1.0),
+    ("ds_bf16_128256", (40,), 128256, torch.bfloat16, 0.7),
+    ("ds_f32_152064", (16,), 152064, torch.float32, 0.8),
+]
+
+
+@pytest.mark.parametrize("name,shape,V,dtype,T", DRAFT_SAMPLE_CASES, ids=[c[0] for c in DRAFT_SAMPLE_CASES])
+def test_draft_sample_parity(lib, name, shape, V, dtype, T):
+    g = torch.Generator().manual_seed(zlib.crc32(name.encode()) % 1000)
+    x = (torch.randn(*shape, V, generator=g) * 4.0).to(dtype)
+    x[..., ::11] = float("-inf")
+    u = torch.rand(*shape, generator=g)
+    ref = oracle.draft_sample_ref(W.as_numpy_logits(x), u.numpy(), T)
+    ws_bytes = lib.workspace_size(int(np.prod(shape)), 0, V,
+                                  lib.DTYPE_BF16 if dtype == torch.bfloat16 else lib.DTYPE_F32,
+                                  lib.MODE_SAMPLE)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    tok, q, status = lib.draft_sample(_dev(x), _dev(u), T, workspace=ws, debug=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    tok, q = tok.cpu().numpy(), q.cpu().numpy()
+    flagged = ref["flags"] != 0
+    assert not ((tok != ref["tokens"]) & ~flagged).any(), (name, int(((tok != ref["tokens"]) & ~flagged).sum()))
+    tol = 1e-5 if dtype == torch.float32 else 2e-3
+    assert np.abs(q - ref["q_at"]).max() <= tol, name
+    assert int(ws.count_nonzero().item()) == 0  # left zero-filled
+
+
+def test_draft_sample_rejects_unaligned_rows(lib):
+    x = torch.randn(4, 1001, device="cuda")  # 4004-byte rows: not 16-byte multiples
+    u = torch.rand(4, device="cuda")
+    with pytest.raises(lib.SpecVerifyError):
+        lib.draft_sample(x, u, 1.0)

@@ -38,7 +38,7 @@ def _header_defines():
 def test_library_exports_every_declared_symbol(binding):
     names = _declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
-                          "spec_status_string", "spec_verify_static"}
+                          "spec_status_string", "spec_verify_static", "spec_draft_sample"}
     assert set(names) == set(binding.EXPORTS)
     lib = ctypes.CDLL(binding.LIB_PATH)
     for n in names:
@@ -150,3 +150,26 @@ def test_python_binding_refuses_cpu_fallback(binding):
     t = torch.zeros((2, 3, 10))
     with pytest.raises(Exception):
         binding._call(t, None, None, None, 1.0, "greedy", False, None, None)
+
+
+def test_draft_sample_host_checks(binding):
+    """spec_draft_sample's argument errors return before any launch (fake,
+    never dereferenced pointers)."""
+    f = binding._lib.spec_draft_sample
+    P, fake = ctypes.c_void_p, ctypes.c_void_p(1 << 20)
+    ws = binding.workspace_size(4, 0, 1024, binding.DTYPE_F32, binding.MODE_SAMPLE)
+    def call(R=4, V=1024, dtype=binding.DTYPE_F32, T=1.0, logits=fake, u=fake, tok=fake, nbytes=ws):
+        return f(logits, u, R, V, dtype, T, tok, None, fake, nbytes, None, None)
+    assert call(R=-1) == binding.ERR_INVALID_ARG
+    assert call(V=0) == binding.ERR_INVALID_ARG
+    assert call(dtype=7) == binding.ERR_INVALID_ARG
+    assert call(T=0.0) == binding.ERR_INVALID_ARG
+    assert call(T=float("nan")) == binding.ERR_INVALID_ARG
+    assert call(logits=None) == binding.ERR_INVALID_ARG
+    assert call(u=None) == binding.ERR_INVALID_ARG
+    assert call(tok=None) == binding.ERR_INVALID_ARG
+    assert call(nbytes=16) == binding.ERR_INVALID_ARG
+    assert call(V=binding.MAX_V + 1) == binding.ERR_UNSUPPORTED
+    wsu = binding.workspace_size(4, 0, 1001, binding.DTYPE_F32, binding.MODE_SAMPLE)
+    assert call(V=1001, nbytes=wsu) == binding.ERR_UNSUPPORTED  # rows not 16-byte multiples
+    assert call(R=0) == binding.OK
