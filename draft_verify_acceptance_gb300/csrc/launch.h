@@ -73,4 +73,12 @@ cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
 cudaError_t launch_sample_early_exit(const VerifyArgs& a, const DeviceInfo& dev, int C,
                                      cudaStream_t stream);
 
+// The drafter's sampling step: one cluster of C CTAs per row, the row staged
+// in shared memory (rows of up to 8 * 96 KiB).
+int row_sample_cluster(long long nvec);
+cudaError_t row_sample_prepare();
+cudaError_t launch_row_sample(const void* logits, const float* uniforms, int R, int V, bool bf16,
+                              float scale, int32_t* tokens, float* q_at, int32_t* status, int C,
+                              cudaStream_t stream);
+
 }  // namespace specv

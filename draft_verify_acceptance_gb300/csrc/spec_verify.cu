@@ -31,6 +31,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     if (e == cudaSuccess) e = sample_prepare();
     if (e == cudaSuccess) e = sample_fused_prepare();
     if (e == cudaSuccess) e = sample_2p_prepare(&d);
+    if (e == cudaSuccess) e = row_sample_prepare();
     g_info[device] = d;
     g_err[device] = e;
   });
@@ -169,8 +170,16 @@ spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R
   specv::DeviceInfo info;
   if (specv::device_info(dev, &info) != cudaSuccess) return SPEC_ERR_CUDA;
 
-  // a verify of R sequences with K = 0: its one draw is the bonus draw from
-  // p_0 = softmax(row / T) with u[r], and p_emit is p_0 at the drawn token
+  const float scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  const int C = specv::row_sample_cluster(rowbytes / 16);
+  if (C > 0) {  // rows that fit a cluster's shared memory: read once
+    const cudaError_t e = specv::launch_row_sample(
+        logits, uniforms, R, V, dtype == SPEC_DTYPE_BF16, scale, tokens, q_at, device_status, C,
+        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  }
+  // longer rows: a verify of R sequences with K = 0, whose one draw is the
+  // bonus draw from p_0 = softmax(row / T) with u[r]; p_emit is p_0 there
   specv::VerifyArgs a;
   a.target = logits;
   a.draft = nullptr;
@@ -181,7 +190,7 @@ spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R
   a.V = V;
   a.bf16 = dtype == SPEC_DTYPE_BF16;
   a.vec = true;
-  a.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.scale = scale;
   a.accepted_len = nullptr;
   a.out_tokens = tokens;
   a.p_at = nullptr;
