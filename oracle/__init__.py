@@ -24,6 +24,7 @@ VARIANT_LITERAL_TARGET = 1  # negative control: correction drawn from p_n
 DATA_TOKEN = 1
 DATA_LOGIT = 2
 DATA_UNIFORM = 4
+DATA_SCORE = 8
 
 FLAG_RATIO = 1
 FLAG_CDF = 2
@@ -45,6 +46,9 @@ def _load():
         lib.spec_oracle_draft_sample.restype = ctypes.c_int
         lib.spec_oracle_draft_sample.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_double, P, P, P, P]
+        lib.spec_oracle_rejection_cut.restype = ctypes.c_int
+        lib.spec_oracle_rejection_cut.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                  P, P, P, P]
         lib.spec_oracle_softmax.restype = ctypes.c_int
         lib.spec_oracle_softmax.argtypes = [P, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, P]
@@ -129,6 +133,27 @@ def draft_sample_ref(logits, uniforms, temperature=1.0):
     shape = t.shape[:-1]
     return {"tokens": tok.reshape(shape), "q_at": q.reshape(shape),
             "flags": flags.reshape(shape), "status": status.value}
+
+
+def rejection_cut_ref(scores, alpha):
+    """Speculative Rejection's cut over G prompts of N reward scores each.
+    scores [G, N] float32, alpha in [0, 1].  Returns r_cut [G] (float64),
+    n_accepted [G] (int32), accepted [G, N] (int32, ascending indices of the
+    kept sequences, then -1) and status."""
+    lib = _load()
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    if s.ndim != 2:
+        raise ValueError("scores must be [G, N]")
+    G, N = s.shape
+    r = np.empty(G, np.float64)
+    n = np.empty(G, np.int32)
+    acc = np.empty((G, N), np.int32)
+    status = ctypes.c_int32(0)
+    rc = lib.spec_oracle_rejection_cut(_ptr(s), G, N, float(alpha), _ptr(r), _ptr(n), _ptr(acc),
+                                       ctypes.byref(status))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return {"r_cut": r, "n_accepted": n, "accepted": acc, "status": status.value}
 
 
 def softmax_ref(row, temperature=1.0):

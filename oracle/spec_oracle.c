@@ -21,6 +21,10 @@
  *   [BPD]  "Garden | Blockwise Parallel Decoding", sections 3.2 and 3.5
  *          (greedy verify: longest prefix where draft == argmax(target),
  *          then the target's own token at the first mismatch).
+ *   [SR]   "Speculative Rejection" review (AI闲谈), section 4.2 "算法", the
+ *          speculative-rejection phase: the cut r_cut is the alpha-quantile
+ *          of the partial reward scores and the sequences scoring at least
+ *          r_cut go on to the next round.
  *
  * Readings where the pages are silent or garbled (each is listed with its
  * reason in the design notes):
@@ -63,7 +67,8 @@ enum {
 enum {
   ORACLE_DATA_TOKEN = 1,     /* draft token outside [0, V)               */
   ORACLE_DATA_LOGIT = 2,     /* NaN / +inf logit, or a row with no mass  */
-  ORACLE_DATA_UNIFORM = 4    /* uniform outside [0, 1) or NaN            */
+  ORACLE_DATA_UNIFORM = 4,   /* uniform outside [0, 1) or NaN            */
+  ORACLE_DATA_SCORE = 8      /* NaN / infinite reward score (rejection cut) */
 };
 /* boundary flags, per sequence (sampling mode only) */
 enum {
@@ -361,6 +366,66 @@ int spec_oracle_draft_sample(const void* logits, const float* uniforms, int R, i
     if (flags) flags[r] = fl;
     total |= st;
     free(p);
+  }
+  if (status) *status = total;
+  return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Ascending order of doubles for qsort. */
+static int cmp_double(const void* a, const void* b) {
+  const double x = *(const double*)a, y = *(const double*)b;
+  return (x > y) - (x < y);
+}
+
+/* Speculative Rejection's cut ([SR] 4.2, the speculative-rejection phase),
+ * for G independent prompts of N partial reward scores each (scores [G, N]).
+ *
+ * Readings: the alpha-quantile is the usual one of sorted samples with
+ * linear interpolation between neighbouring order statistics (position
+ * h = alpha * (N - 1), 0-based), and a sequence is kept when its score is
+ * at least r_cut.  So, per prompt, with s the scores sorted ascending,
+ *   j = floor(h), g = h - j, r_cut = s[j] + g * (s[min(j + 1, N - 1)] - s[j])
+ * in IEEE double (no fused multiply-add), and accepted[] lists, in ascending
+ * order, every index k with scores[k] >= r_cut; the rest of the row is -1.
+ * A prompt with a NaN or infinite score sets ORACLE_DATA_SCORE in *status
+ * and gets r_cut = NaN, n_accepted = 0 and a row of -1. */
+int spec_oracle_rejection_cut(const float* scores, int G, int N, double alpha, double* r_cut,
+                              int32_t* n_accepted, int32_t* accepted, int32_t* status) {
+  if (G < 0 || N < 0 || !(alpha >= 0.0 && alpha <= 1.0)) return ORACLE_ERR_INVALID_ARG;
+  if (G == 0) { if (status) *status = 0; return ORACLE_OK; }
+  if (N < 1 || !scores || !r_cut || !n_accepted || !accepted) return ORACLE_ERR_INVALID_ARG;
+  const double h = alpha * (double)(N - 1);
+  const double jf = floor(h);
+  const int j = (int)jf;
+  const double g = h - jf;
+  int total = 0, nomem = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : total) reduction(| : nomem)
+  for (int pr = 0; pr < G; ++pr) {
+    const float* row = scores + (size_t)pr * (size_t)N;
+    int32_t* out = accepted + (size_t)pr * (size_t)N;
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!s) { nomem = 1; continue; }
+    int bad = 0;
+    for (int k = 0; k < N; ++k) {
+      s[k] = (double)row[k];
+      if (!isfinite(s[k])) bad = 1;
+    }
+    int n = 0;
+    if (bad) {
+      r_cut[pr] = NAN;
+      total |= ORACLE_DATA_SCORE;
+    } else {
+      qsort(s, (size_t)N, sizeof(double), cmp_double);
+      const double lo = s[j];
+      const double hi = s[j + 1 < N ? j + 1 : N - 1];
+      const double r = lo + g * (hi - lo);
+      r_cut[pr] = r;
+      for (int k = 0; k < N; ++k)
+        if ((double)row[k] >= r) out[n++] = k;
+    }
+    n_accepted[pr] = n;
+    for (int k = n; k < N; ++k) out[k] = -1;
+    free(s);
   }
   if (status) *status = total;
   return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;

@@ -571,3 +571,115 @@ def test_draft_sample_data_errors():
     u = np.array([0.5, 0.5, 1.5], np.float32)
     r = oracle.draft_sample_ref(x, u, 1.0)
     assert r["status"] == oracle.DATA_LOGIT | oracle.DATA_UNIFORM
+
+
+# --------------------------------------------------------------------------
+# Speculative Rejection's cut ("Speculative Rejection" review, section 4.2,
+# the speculative-rejection phase): r_cut is the alpha-quantile of the
+# partial reward scores and the sequences scoring at least r_cut are kept.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("N", [1, 2, 7, 1000])
+@pytest.mark.parametrize("alpha", [0.0, 0.1, 0.5, 0.731, 0.9, 1.0])
+def test_rejection_cut_is_the_library_quantile(N, alpha):
+    rng = np.random.default_rng(N * 31 + int(alpha * 1000))
+    s = rng.standard_normal((32, N)).astype(np.float32)
+    res = oracle.rejection_cut_ref(s, alpha)
+    assert res["status"] == 0
+    for g in range(s.shape[0]):
+        row = s[g].astype(np.float64)
+        q = np.quantile(row, alpha)  # linear interpolation between order statistics
+        np.testing.assert_allclose(res["r_cut"][g], q, rtol=1e-12, atol=0)
+        # no score sits within rounding of the cut, so the kept set is unique
+        near = np.abs(row - q) <= 1e-9 * max(1.0, abs(q))
+        exact_hits = row == res["r_cut"][g]
+        assert not np.any(near & ~exact_hits)
+        want = np.flatnonzero(row >= res["r_cut"][g])
+        n = res["n_accepted"][g]
+        assert n == want.size
+        np.testing.assert_array_equal(res["accepted"][g, :n], want)
+        assert np.all(res["accepted"][g, n:] == -1)
+
+
+@pytest.mark.parametrize("N", [2, 5, 65, 1025])
+def test_rejection_cut_on_the_order_statistic_grid(N):
+    """alpha = k / (N - 1) puts the quantile exactly on the k-th smallest
+    score; with distinct scores the cut keeps exactly N - k sequences.  N - 1
+    is a power of two so that alpha * (N - 1) is exactly k in double."""
+    rng = np.random.default_rng(N)
+    perm = rng.permutation(N).astype(np.float32) * 0.5 - 7.0
+    s = perm[None, :]
+    for k in sorted({0, 1, N // 3, N // 2, N - 2, N - 1}):
+        res = oracle.rejection_cut_ref(s, k / (N - 1))
+        assert res["r_cut"][0] == k * 0.5 - 7.0
+        assert res["n_accepted"][0] == N - k
+        np.testing.assert_array_equal(res["accepted"][0, :N - k], np.flatnonzero(perm >= k * 0.5 - 7.0))
+
+
+def test_rejection_cut_worked_by_hand():
+    s = np.array([[3, 1, 4, 1, 5]], np.float32)  # sorted: 1 1 3 4 5
+    cases = {0.5: (3.0, [0, 2, 4]),     # h = 2: the middle score, kept itself
+             0.25: (1.0, [0, 1, 2, 3, 4]),  # h = 1: both ones tie with the cut
+             0.6: (3.4, [2, 4]),        # h = 2.4: 3 + 0.4 * (4 - 3)
+             1.0: (5.0, [4]),           # the best score alone
+             0.0: (1.0, [0, 1, 2, 3, 4])}
+    for alpha, (r, kept) in cases.items():
+        res = oracle.rejection_cut_ref(s, alpha)
+        assert res["r_cut"][0] == pytest.approx(r, rel=1e-15)
+        n = res["n_accepted"][0]
+        assert list(res["accepted"][0, :n]) == kept
+        assert list(res["accepted"][0, n:]) == [-1] * (5 - n)
+
+
+def test_rejection_cut_ties_keep_every_equal_score():
+    s = np.full((3, 9), 2.5, np.float32)
+    s[1, ::2] = -1.0  # 5 of -1, 4 of 2.5
+    s[2] = np.array([0, 0, 1, 1, 1, 2, 2, 2, 2], np.float32)
+    for alpha in [0.0, 0.3, 0.5, 0.99, 1.0]:
+        res = oracle.rejection_cut_ref(s, alpha)
+        assert res["n_accepted"][0] == 9
+        for g in (1, 2):
+            row = s[g].astype(np.float64)
+            q = np.quantile(row, alpha)
+            assert res["r_cut"][g] == pytest.approx(q, rel=1e-15, abs=1e-300)
+            n = res["n_accepted"][g]
+            np.testing.assert_array_equal(res["accepted"][g, :n], np.flatnonzero(row >= res["r_cut"][g]))
+
+
+def test_rejection_cut_invariants():
+    """More pruning never keeps more sequences; every kept score is at least
+    every dropped one; the best sequence is always kept."""
+    rng = np.random.default_rng(5)
+    s = (rng.standard_normal((16, 257)) * 3).astype(np.float32)
+    prev = None
+    for alpha in np.linspace(0.0, 1.0, 21):
+        res = oracle.rejection_cut_ref(s, alpha)
+        n = res["n_accepted"]
+        assert np.all(n >= 1)
+        if prev is not None:
+            assert np.all(n <= prev)
+        prev = n
+        for g in range(s.shape[0]):
+            keep = res["accepted"][g, :n[g]]
+            mask = np.zeros(s.shape[1], bool)
+            mask[keep] = True
+            assert np.argmax(s[g]) in keep
+            if (~mask).any():
+                assert s[g][mask].min() >= s[g][~mask].max()
+
+
+def test_rejection_cut_data_errors_and_shapes():
+    s = np.zeros((4, 6), np.float32)
+    s[1, 3] = np.nan
+    s[2, 0] = np.inf
+    res = oracle.rejection_cut_ref(s, 0.5)
+    assert res["status"] == oracle.DATA_SCORE
+    assert list(res["n_accepted"]) == [6, 0, 0, 6]
+    assert np.isnan(res["r_cut"][1]) and np.isnan(res["r_cut"][2])
+    assert np.all(res["accepted"][1] == -1) and np.all(res["accepted"][2] == -1)
+    for bad in (-0.1, 1.5, float("nan")):
+        with pytest.raises(ValueError):
+            oracle.rejection_cut_ref(s, bad)
+    with pytest.raises(ValueError):
+        oracle.rejection_cut_ref(np.zeros((2, 0), np.float32), 0.5)
+    empty = oracle.rejection_cut_ref(np.zeros((0, 5), np.float32), 0.5)
+    assert empty["status"] == 0 and empty["n_accepted"].size == 0
