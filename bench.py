@@ -167,6 +167,7 @@ KERNEL_SOURCES = {
     "norm_stream_kernel": ["verify_sample_2p.cu", "sample_common.cuh", "device_common.cuh",
                            "launch.h"],
     "sample_kernel": ["verify_sample.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
+    "cut_warp_kernel": ["rejection_cut.cu", "launch.h"],
 }
 
 
@@ -386,7 +387,56 @@ def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
         if inp.mode == W.MODE_SAMPLE and inp.K > 0:
             table[name + "+early_exit"] = early_exit_line(binding, inp, steps, dev, l2, peak, sec)
             table[name + "+draft_sample"] = draft_sample_line(binding, inp, steps, dev, l2, peak)
+    for name, spec in W.REJECTION_WORKLOADS.items():
+        table[name] = rejection_cut_line(binding, spec, steps, dev, l2, peak)
     return table
+
+
+def rejection_cut_line(binding, spec, steps, dev, l2, peak):
+    """Speculative Rejection's cut over G prompts of N scores (bytes: the
+    scores read, the kept-index rows, r_cut and the counts written),
+    graph-replayed over rotating score copies > 2x L2; the oracle's time on
+    the same batch beside it."""
+    import torch
+    from draft_verify_acceptance_gb300 import workloads as W
+    G, N, alpha = spec["G"], spec["N"], spec["alpha"]
+    scores = W.make_scores(G, N, kind=spec["kind"], seed=0)
+    nbytes = G * N * 4 * 2 + G * (8 + 4)
+    R = min(64, max(2, math.ceil(2 * l2 / max(nbytes, 1)) + 1))
+    copies = [scores.to(dev) for _ in range(R)]
+    out = (torch.empty(G, dtype=torch.float64, device=dev),
+           torch.empty(G, dtype=torch.int32, device=dev),
+           torch.empty((G, N), dtype=torch.int32, device=dev))
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for r in range(3):
+            binding.rejection_cut(copies[r % R], alpha, stream=stream, out=out)
+        stream.synchronize()
+        n = min(steps, 1000)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n):
+                binding.rejection_cut(copies[k % R], alpha, stream=stream, out=out)
+        g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    del g, copies
+    torch.cuda.empty_cache()
+    import oracle
+    t0 = time.perf_counter()
+    oracle.rejection_cut_ref(scores.numpy(), alpha)
+    cpu_sec = time.perf_counter() - t0
+    return {"us_per_step": sec * 1e6, "scores_per_s": G * N / sec, "bytes": nbytes,
+            "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
+            "kernel": "cut_warp_kernel" if N <= 1024 else "cut_block_kernel",
+            "cpu_baseline": {"value": G * N / cpu_sec, "unit": "scores/s",
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"the whole batch ({G} x {N}), once"}}
 
 
 def draft_sample_line(binding, inp, steps, dev, l2, peak):

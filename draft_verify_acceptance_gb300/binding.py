@@ -34,11 +34,12 @@ DATA_TOKEN_RANGE = 1
 DATA_NONFINITE_LOGIT = 2
 DATA_UNIFORM_RANGE = 4
 DEVICE_WAIT_TIMEOUT = 8
+DATA_NONFINITE_SCORE = 16
 FLAG_RATIO = 1
 FLAG_CDF = 2
 
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_status_string",
-           "spec_verify_static", "spec_draft_sample")
+           "spec_verify_static", "spec_draft_sample", "spec_rejection_cut")
 
 
 class SpecVerifyError(RuntimeError):
@@ -64,6 +65,8 @@ def _load():
     lib.spec_verify_static.argtypes = [P, P, P, P, I, I, I, I, F, I, P, P, P]
     lib.spec_draft_sample.restype = I
     lib.spec_draft_sample.argtypes = [P, P, I, I, I, F, P, P, P, Z, P, P]
+    lib.spec_rejection_cut.restype = I
+    lib.spec_rejection_cut.argtypes = [P, I, I, ctypes.c_double, P, P, P, P, P]
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [I]
     return lib
@@ -243,6 +246,37 @@ def draft_sample(logits, uniforms, temperature=1.0, *, stream=None, workspace=No
     if rc != OK:
         raise SpecVerifyError(rc, "spec_draft_sample")
     return (tokens, q_at, status) if debug else (tokens, q_at)
+
+
+def rejection_cut(scores, alpha, *, stream=None, out=None, debug=False):
+    """Speculative Rejection's cut on the GPU: for each prompt (row of
+    ``scores``, [G, N] float32, CUDA) r_cut = the alpha-quantile of its N
+    reward scores, and the indices scoring at least r_cut.  Returns (r_cut
+    float64 [G], n_accepted int32 [G], accepted int32 [G, N]: kept indices in
+    ascending order then -1), plus the status word when ``debug``, queued on
+    ``stream``; ``out`` may give those three tensors preallocated."""
+    if scores is None or scores.dim() != 2:
+        raise ValueError("scores must be [G, N]")
+    device = scores.device
+    G, N = scores.shape
+    _check(scores, "scores", (torch.float32,), (G, N), device)
+    stream = stream or torch.cuda.current_stream(device)
+    if out is not None:
+        r_cut, n_acc, acc = out
+        _check(r_cut, "r_cut", (torch.float64,), (G,), device)
+        _check(n_acc, "n_accepted", (torch.int32,), (G,), device)
+        _check(acc, "accepted", (torch.int32,), (G, N), device)
+    else:
+        r_cut = torch.empty(G, dtype=torch.float64, device=device)
+        n_acc = torch.empty(G, dtype=torch.int32, device=device)
+        acc = torch.empty((G, N), dtype=torch.int32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device) if debug else None
+    with torch.cuda.device(device):
+        rc = _lib.spec_rejection_cut(_ptr(scores), G, N, float(alpha), _ptr(r_cut), _ptr(n_acc),
+                                     _ptr(acc), ctypes.c_void_p(stream.cuda_stream), _ptr(status))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_rejection_cut")
+    return (r_cut, n_acc, acc, status) if debug else (r_cut, n_acc, acc)
 
 
 def _verify_host(target, draft, tokens, uniforms, temperature, mode, stream):

@@ -81,4 +81,10 @@ cudaError_t launch_row_sample(const void* logits, const float* uniforms, int R, 
                               float scale, int32_t* tokens, float* q_at, int32_t* status, int C,
                               cudaStream_t stream);
 
+// Speculative Rejection's cut: r_cut and the kept indices per prompt
+// (j, g from alpha (N - 1) on the host).
+cudaError_t launch_rejection_cut(const float* scores, int G, int N, int j, double g,
+                                 double* r_cut, int32_t* n_accepted, int32_t* accepted,
+                                 int32_t* status, cudaStream_t stream);
+
 }  // namespace specv

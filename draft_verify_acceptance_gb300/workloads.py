@@ -15,6 +15,12 @@ Recipe (torch CPU generator, one stream per input, drawn in this order):
   stream 3: uniforms       u[B, K+1] ~ U[0, 1), fp32
 Stream k of seed s is ``torch.Generator().manual_seed(16 * s + k)``.
 Logits are cast to the workload dtype (fp32 or bf16) once and then frozen.
+
+Reward scores for Speculative Rejection's cut (``make_scores``, stream 4):
+prompt g gets a shift mu_g = 2 * N(0,1) and a spread sigma_g = exp(0.5 * N(0,1))
+(reward distributions differ a lot between prompts), and its N partial scores
+are mu_g + sigma_g * N(0,1) in fp32; kind "ties" draws integers in [-3, 3]
+instead (many equal scores, signed zeros included).
 """
 from dataclasses import dataclass, field
 from typing import Optional
@@ -115,6 +121,29 @@ WORKLOADS = {
     "long_draft_f32_B16_K16_V152064_T0.8": dict(
         B=16, K=16, V=152064, dtype=torch.float32, mode=MODE_SAMPLE, temperature=0.8,
         target_std=5.0, independent_draft=True),
+}
+
+
+def make_scores(G: int, N: int, *, kind: str = "normal", seed: int = 0) -> torch.Tensor:
+    """[G, N] float32 partial reward scores following the recipe above."""
+    g = _gen(seed, 4)
+    if kind == "normal":
+        mu = 2.0 * torch.randn((G, 1), generator=g, dtype=torch.float64)
+        sigma = torch.exp(0.5 * torch.randn((G, 1), generator=g, dtype=torch.float64))
+        z = torch.randn((G, N), generator=g, dtype=torch.float64)
+        return (mu + sigma * z).to(torch.float32).contiguous()
+    if kind == "ties":
+        v = torch.randint(-3, 4, (G, N), generator=g).to(torch.float32)
+        neg0 = torch.rand((G, N), generator=g) < 0.5
+        return torch.where((v == 0) & neg0, torch.full_like(v, -0.0), v).contiguous()
+    raise ValueError(f"unknown score kind {kind!r}")
+
+
+# Speculative Rejection's cut: G prompts of N = 1000 scored partial responses
+# (the number of responses per prompt the review's Figure 2 uses), cut at
+# alpha = 0.5.
+REJECTION_WORKLOADS = {
+    "rejection_cut_f32_G16384_N1000_a0.5": dict(G=16384, N=1000, alpha=0.5, kind="normal"),
 }
 
 

@@ -79,6 +79,7 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 /* Not a data error: a kernel's bounded wait for its own bulk copies gave up
  * (outputs of that call are unspecified).  Never expected in normal use. */
 #define SPEC_DEVICE_WAIT_TIMEOUT 8
+#define SPEC_DATA_NONFINITE_SCORE 16 /* spec_rejection_cut: a NaN or infinite score */
 
 /* Per-sequence boundary flags (sampling mode; written when `flags` is given).
  * They mark decisions the kernel took within 1e-6 of a threshold, where a
@@ -241,6 +242,40 @@ SPEC_API spec_status_t spec_draft_sample(const void* logits, const float* unifor
                                          int dtype, float temperature, int32_t* tokens,
                                          float* q_at, void* workspace, size_t workspace_bytes,
                                          spec_stream_t stream, int32_t* device_status);
+
+/*
+ * spec_rejection_cut -- Speculative Rejection's cut (review "Speculative
+ * Rejection", section 4.2 "算法", the speculative-rejection phase: the
+ * partial responses are scored, r_cut is the alpha-quantile of the scores,
+ * and the sequences scoring at least r_cut are kept for the next round).
+ * For each of G prompts independently, with s its N scores sorted ascending:
+ *
+ *   h = alpha * (N - 1),  j = floor(h),  g = h - j,
+ *   r_cut = s[j] + g * (s[min(j + 1, N - 1)] - s[j])     (IEEE double, no FMA)
+ *   kept  = { k : (double)scores[k] >= r_cut }            (never empty)
+ *
+ * which is the usual sample quantile with linear interpolation between
+ * neighbouring order statistics.
+ *
+ *   scores      [G, N] fp32, device, 4-byte aligned.
+ *   G, N        G >= 0 (G == 0 is a no-op), N >= 1 when G > 0.
+ *   alpha       in [0, 1] (the termination ratio): 0 keeps every sequence,
+ *               1 keeps the best-scoring ones only.
+ *   r_cut       [G] double out, device, 8-byte aligned.
+ *   n_accepted  [G] int32 out, device: the number of kept sequences.
+ *   accepted    [G, N] int32 out, device: row g lists the kept indices of
+ *               prompt g in ascending order, then -1 up to N.
+ *   device_status  int32 in/out or NULL: a prompt with a NaN or infinite
+ *               score ORs SPEC_DATA_NONFINITE_SCORE into it and gets
+ *               r_cut = NaN, n_accepted = 0 and a row of -1.
+ *
+ * No workspace.  Asynchronous on `stream`; argument errors (negative sizes,
+ * N == 0 with G > 0, alpha outside [0, 1] or NaN, a NULL or misaligned
+ * pointer) return SPEC_ERR_INVALID_ARG before any launch.
+ */
+SPEC_API spec_status_t spec_rejection_cut(const float* scores, int G, int N, double alpha,
+                                          double* r_cut, int32_t* n_accepted, int32_t* accepted,
+                                          spec_stream_t stream, int32_t* device_status);
 
 /* A short, static, human-readable description of a return code. */
 SPEC_API const char* spec_status_string(int status);

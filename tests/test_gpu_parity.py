@@ -369,3 +369,95 @@ def test_draft_sample_rejects_unaligned_rows(lib):
     u = torch.rand(4, device="cuda")
     with pytest.raises(lib.SpecVerifyError):
         lib.draft_sample(x, u, 1.0)
+
+
+# --------------------------------------------------------------------------
+# Speculative Rejection's cut: r_cut, the kept count and the kept indices are
+# bit-equal to the oracle's (r_cut is one fixed double expression of two
+# order statistics, and the keep test is exact).
+# --------------------------------------------------------------------------
+CUT_CASES = [
+    # (name, G, N, alpha, score kind): warp kernel (N <= 1024, four register
+    # widths, ragged G and N), block kernel (N > 1024), ties, alpha edges
+    ("cut_n1", 3, 1, 0.5, "normal"),
+    ("cut_n5", 17, 5, 0.6, "normal"),
+    ("cut_n100", 33, 100, 0.25, "normal"),
+    ("cut_n200_ties", 40, 200, 0.5, "ties"),
+    ("cut_n513", 9, 513, 0.9, "normal"),
+    ("cut_n1000", 1001, 1000, 0.5, "normal"),
+    ("cut_n1000_a0", 50, 1000, 0.0, "normal"),
+    ("cut_n1000_a1", 50, 1000, 1.0, "normal"),
+    ("cut_n1000_tiny_g", 64, 1000, 1e-300, "ties"),
+    ("cut_n1024_ties", 16, 1024, 0.731, "ties"),
+    ("cut_n1025", 7, 1025, 0.5, "normal"),
+    ("cut_n5000_ties", 5, 5000, 0.3, "ties"),
+    ("cut_n70000", 2, 70000, 0.77, "normal"),
+]
+
+
+def _assert_cut_equal(got, ref, name):
+    r, n, acc = (t.cpu().numpy() for t in got)
+    np.testing.assert_array_equal(np.isnan(r), np.isnan(ref["r_cut"]), err_msg=name)
+    ok = ~np.isnan(r)
+    assert np.array_equal(r[ok], ref["r_cut"][ok]), (name, np.flatnonzero(r[ok] != ref["r_cut"][ok])[:5])
+    np.testing.assert_array_equal(n, ref["n_accepted"], err_msg=name)
+    np.testing.assert_array_equal(acc, ref["accepted"], err_msg=name)
+
+
+@pytest.mark.parametrize("name,G,N,alpha,kind", CUT_CASES, ids=[c[0] for c in CUT_CASES])
+def test_rejection_cut_parity(lib, name, G, N, alpha, kind):
+    s = W.make_scores(G, N, kind=kind, seed=zlib.crc32(name.encode()) % 1000)
+    ref = oracle.rejection_cut_ref(s.numpy(), alpha)
+    got = lib.rejection_cut(_dev(s), alpha, debug=True)
+    torch.cuda.synchronize()
+    assert int(got[3].item()) == 0
+    _assert_cut_equal(got[:3], ref, name)
+
+
+@pytest.mark.parametrize("N", [100, 1000, 2000])
+def test_rejection_cut_extreme_scores(lib, N):
+    """Scores at the ends of the fp32 range (keys next to the padding of a
+    ragged row), all-equal rows and tiny spreads."""
+    s = W.make_scores(24, N, seed=N + 1)
+    s[0] = -3.0e38
+    s[1, : N // 2] = -3.0e38
+    s[2, ::3] = 3.0e38
+    s[3] = 1e-40  # subnormal, all equal
+    s[4] = s[4] * 1e-30
+    s[5, ::2] = -0.0
+    s[5, 1::2] = 0.0
+    for alpha in (0.0, 0.37, 1.0):
+        ref = oracle.rejection_cut_ref(s.numpy(), alpha)
+        got = lib.rejection_cut(_dev(s), alpha)
+        torch.cuda.synchronize()
+        _assert_cut_equal(got, ref, f"extreme N={N} alpha={alpha}")
+
+
+def test_rejection_cut_full_size(lib):
+    """The benchmarked workload (16384 prompts of 1000 scores), every output."""
+    spec = W.REJECTION_WORKLOADS["rejection_cut_f32_G16384_N1000_a0.5"]
+    s = W.make_scores(spec["G"], spec["N"], kind=spec["kind"], seed=0)
+    ref = oracle.rejection_cut_ref(s.numpy(), spec["alpha"])
+    got = lib.rejection_cut(_dev(s), spec["alpha"])
+    torch.cuda.synchronize()
+    _assert_cut_equal(got, ref, "full")
+
+
+@pytest.mark.parametrize("N", [300, 3000])
+def test_rejection_cut_nonfinite_scores(lib, N):
+    s = W.make_scores(12, N, seed=N)
+    s[2, 7] = float("nan")
+    s[5, N - 1] = float("inf")
+    s[9, 0] = float("-inf")
+    ref = oracle.rejection_cut_ref(s.numpy(), 0.4)
+    got = lib.rejection_cut(_dev(s), 0.4, debug=True)
+    torch.cuda.synchronize()
+    assert ref["status"] == oracle.DATA_SCORE  # the two sides number their bits on their own
+    assert int(got[3].item()) == lib.DATA_NONFINITE_SCORE
+    _assert_cut_equal(got[:3], ref, f"nonfinite N={N}")
+
+
+def test_rejection_cut_empty_batch(lib):
+    r, n, acc = lib.rejection_cut(torch.zeros((0, 10), device="cuda"), 0.5)
+    torch.cuda.synchronize()
+    assert r.numel() == 0 and n.numel() == 0 and acc.numel() == 0

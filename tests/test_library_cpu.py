@@ -38,7 +38,8 @@ def _header_defines():
 def test_library_exports_every_declared_symbol(binding):
     names = _declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
-                          "spec_status_string", "spec_verify_static", "spec_draft_sample"}
+                          "spec_status_string", "spec_verify_static", "spec_draft_sample",
+                          "spec_rejection_cut"}
     assert set(names) == set(binding.EXPORTS)
     lib = ctypes.CDLL(binding.LIB_PATH)
     for n in names:
@@ -173,3 +174,26 @@ def test_draft_sample_host_checks(binding):
     wsu = binding.workspace_size(4, 0, 1001, binding.DTYPE_F32, binding.MODE_SAMPLE)
     assert call(V=1001, nbytes=wsu) == binding.ERR_UNSUPPORTED  # rows not 16-byte multiples
     assert call(R=0) == binding.OK
+
+
+def test_rejection_cut_host_checks(binding):
+    """spec_rejection_cut's argument errors return before any launch (fake,
+    never dereferenced pointers); G == 0 is a no-op."""
+    f = binding._lib.spec_rejection_cut
+    fake = ctypes.c_void_p(1 << 20)
+    def call(G=4, N=1000, alpha=0.5, s=fake, r=fake, n=fake, acc=fake, st=None):
+        return f(s, G, N, alpha, r, n, acc, None, st)
+    assert binding.DATA_NONFINITE_SCORE == _header_defines()["SPEC_DATA_NONFINITE_SCORE"]
+    assert call(G=-1) == binding.ERR_INVALID_ARG
+    assert call(N=0) == binding.ERR_INVALID_ARG
+    assert call(N=-3) == binding.ERR_INVALID_ARG
+    for a in (-0.01, 1.01, float("nan"), float("inf")):
+        assert call(alpha=a) == binding.ERR_INVALID_ARG
+    assert call(s=None) == binding.ERR_INVALID_ARG
+    assert call(r=None) == binding.ERR_INVALID_ARG
+    assert call(n=None) == binding.ERR_INVALID_ARG
+    assert call(acc=None) == binding.ERR_INVALID_ARG
+    assert call(r=ctypes.c_void_p((1 << 20) + 4)) == binding.ERR_INVALID_ARG  # r_cut: 8-byte aligned
+    assert call(s=ctypes.c_void_p((1 << 20) + 2)) == binding.ERR_INVALID_ARG
+    assert call(st=ctypes.c_void_p((1 << 20) + 1)) == binding.ERR_INVALID_ARG
+    assert call(G=0, N=0) == binding.OK
