@@ -46,6 +46,10 @@ def _load():
         lib.spec_oracle_draft_sample.restype = ctypes.c_int
         lib.spec_oracle_draft_sample.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_double, P, P, P, P]
+        lib.spec_oracle_scd_verify.restype = ctypes.c_int
+        lib.spec_oracle_scd_verify.argtypes = [
+            P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_double, ctypes.c_double, P, P, P, P, P, P]
         lib.spec_oracle_rejection_cut.restype = ctypes.c_int
         lib.spec_oracle_rejection_cut.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                                   P, P, P, P]
@@ -102,6 +106,38 @@ def verify_ref(target, draft, tokens, uniforms, temperature=1.0,
                                 float(temperature), mode, variant, _ptr(n), _ptr(out),
                                 _ptr(p_at), _ptr(q_at), _ptr(flags),
                                 ctypes.byref(status))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    res = {"accepted_len": n, "out_tokens": out, "status": status.value}
+    if want_debug:
+        res.update(p_at=p_at, q_at=q_at, flags=flags)
+    return res
+
+
+def scd_verify_ref(target, amateur, tokens, uniforms, temperature=1.0, alpha=0.1,
+                   want_debug=False):
+    """Speculative contrastive decoding over a batch: target and amateur
+    [B, K+1, V] (float32, or bf16 bits as uint16), tokens [B, K] int32,
+    uniforms [B, K+1] float32, alpha the plausibility cut.  Returns the same
+    dict as verify_ref (p_at is P_n(x_i), q_at the amateur's q(x_i))."""
+    lib = _load()
+    t, dt = _logits(target, "target")
+    B, K1, V = t.shape
+    K = K1 - 1
+    a, adt = _logits(amateur, "amateur")
+    if adt != dt or a.shape != t.shape:
+        raise TypeError("target and amateur must match in dtype and shape")
+    x = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, K + 1)
+    n = np.empty(B, np.int32)
+    out = np.empty((B, K + 1), np.int32)
+    p_at = np.zeros((B, K), np.float64) if want_debug else None
+    q_at = np.zeros((B, K), np.float64) if want_debug else None
+    flags = np.zeros(B, np.uint32) if want_debug else None
+    status = ctypes.c_int32(0)
+    rc = lib.spec_oracle_scd_verify(_ptr(t), _ptr(a), _ptr(x), _ptr(u), B, K, V, dt,
+                                    float(temperature), float(alpha), _ptr(n), _ptr(out),
+                                    _ptr(p_at), _ptr(q_at), _ptr(flags), ctypes.byref(status))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     res = {"accepted_len": n, "out_tokens": out, "status": status.value}

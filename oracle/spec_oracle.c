@@ -44,6 +44,12 @@
  *   - temperature divides both the target and the draft logits.
  *   - greedy: argmax of the raw logit values (bf16 widens exactly), lowest
  *     index on ties.
+ *   - contrastive target ([SCD] "Speculative Contrastive Decoding"; the
+ *     formula was lost from the page, so parity of P_n itself is unpinned):
+ *     contrastive decoding's log p_e - log p_a over the plausible head
+ *     { p_e >= alpha * max p_e }, normalised there (contrastive_row); the
+ *     amateur supplies the draft distribution q and its row K enters only
+ *     P_n,K; replacement and bonus come from P_n as in the plain verify.
  */
 #include <math.h>
 #include <stdint.h>
@@ -243,6 +249,140 @@ static int verify_one_sample(const void* target, const void* draft, const int32_
   return 0;
 }
 
+/* The contrastive target of one position ([SCD] "Speculative Contrastive
+ * Decoding": the expert's distribution replaced by the contrastive-decoding
+ * distribution P_n of the expert Me and the amateur Ma; the formula itself
+ * did not survive on the page, so this is the plain reading of contrastive
+ * decoding):
+ *   head  = { j : t_j > -inf and t_j >= M + L },  M = max_j t_j,
+ *           L = T * ln(alpha)  (p_e(j) >= alpha * max p_e, with p_e =
+ *           softmax(t / T); alpha = 0 gives L = -inf: every finite t_j),
+ *   P_n(j) = exp((t_j - a_j) / T) / Z  on the head, 0 elsewhere
+ *           (log p_e - log p_a up to a constant, normalised over the head).
+ * The caller passes L.  Returns ORACLE_DATA_LOGIT (P all-zero) when either
+ * row holds NaN or +inf, the target row has no finite entry, or a head token
+ * has a_j = -inf (an unbounded contrast). */
+static int contrastive_row(const void* target, const void* amateur, int dtype, size_t off,
+                           int V, double T, double L, double* P) {
+  double M = -INFINITY;
+  int bad = 0;
+  for (int j = 0; j < V; ++j) {
+    const double t = logit_at(target, dtype, off + (size_t)j);
+    const double a = logit_at(amateur, dtype, off + (size_t)j);
+    if (isnan(t) || (isinf(t) && t > 0) || isnan(a) || (isinf(a) && a > 0)) bad = 1;
+    if (t > M) M = t;
+  }
+  const double thr = M + L;
+  double Mc = -INFINITY;
+  if (!bad && M > -INFINITY) {
+    for (int j = 0; j < V; ++j) {
+      const double t = logit_at(target, dtype, off + (size_t)j);
+      if (!(t > -INFINITY && t >= thr)) continue;
+      const double a = logit_at(amateur, dtype, off + (size_t)j);
+      if (!(a > -INFINITY)) { bad = 1; break; }
+      const double c = (t - a) / T;
+      if (c > Mc) Mc = c;
+    }
+  }
+  if (bad || !(M > -INFINITY)) {
+    for (int j = 0; j < V; ++j) P[j] = 0.0;
+    return ORACLE_DATA_LOGIT;
+  }
+  double Z = 0.0;
+  for (int j = 0; j < V; ++j) {
+    const double t = logit_at(target, dtype, off + (size_t)j);
+    if (t > -INFINITY && t >= thr) {
+      const double a = logit_at(amateur, dtype, off + (size_t)j);
+      P[j] = exp((t - a) / T - Mc);
+      Z += P[j];
+    } else {
+      P[j] = 0.0;
+    }
+  }
+  for (int j = 0; j < V; ++j) P[j] /= Z;
+  return 0;
+}
+
+/* One sequence of speculative contrastive decoding ([SCD] "Speculative
+ * Contrastive Decoding"): speculative sampling with the target p_i replaced
+ * by the contrastive P_n,i, including the bonus draw at position K.  The
+ * draft tokens come from the amateur, q_i = softmax(a_i / T); its rows are
+ * a[b, 0..K] (row K only enters P_n,K).  The steps and flags are those of
+ * verify_one_sample. */
+static int scd_one(const void* target, const void* amateur, const int32_t* x, const float* u,
+                   int K, int V, int dtype, double T, double L, size_t b, int32_t* n_out,
+                   int32_t* out, double* p_at, double* q_at, uint32_t* flag_out) {
+  int status = 0;
+  uint32_t flag = 0;
+  for (int i = 0; i < K; ++i)
+    if (x[i] < 0 || x[i] >= V) status |= ORACLE_DATA_TOKEN;
+  for (int i = 0; i <= K; ++i)
+    if (!(u[i] >= 0.0f && u[i] < 1.0f)) status |= ORACLE_DATA_UNIFORM;
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  double* px = (double*)malloc(sizeof(double) * (size_t)(K + 1));
+  double* qx = (double*)malloc(sizeof(double) * (size_t)(K + 1));
+  if (!p || !q || !r || !px || !qx) {
+    free(p); free(q); free(r); free(px); free(qx);
+    return -1;
+  }
+  for (int i = 0; i <= K; ++i) {
+    const size_t off = (b * (size_t)(K + 1) + (size_t)i) * (size_t)V;
+    status |= contrastive_row(target, amateur, dtype, off, V, T, L, p);
+    if (i == K) break;
+    status |= row_softmax(amateur, dtype, off, V, T, q);
+    const int xi = (x[i] >= 0 && x[i] < V) ? x[i] : 0;
+    px[i] = p[xi];
+    qx[i] = q[xi];
+    if (p_at && q_at) {
+      p_at[b * (size_t)K + (size_t)i] = px[i];
+      q_at[b * (size_t)K + (size_t)i] = qx[i];
+    }
+  }
+  if (status) {
+    *n_out = -1;
+    for (int i = 0; i <= K; ++i) out[i] = -1;
+    *flag_out = 0;
+    free(p); free(q); free(r); free(px); free(qx);
+    return status;
+  }
+  int n = K;
+  for (int i = 0; i < K; ++i) {
+    const double ui = (double)u[i];
+    if (qx[i] > 0.0) {
+      double ratio = px[i] / qx[i];
+      if (ratio > 1.0) ratio = 1.0;
+      if (fabs(ui - ratio) < kBand) flag |= ORACLE_FLAG_RATIO;
+    }
+    if (!(ui * qx[i] < px[i])) { n = i; break; }
+  }
+  const double uK = (double)u[K];
+  const size_t off_n = (b * (size_t)(K + 1) + (size_t)n) * (size_t)V;
+  contrastive_row(target, amateur, dtype, off_n, V, T, L, p);
+  int chosen;
+  if (n < K) {
+    row_softmax(amateur, dtype, off_n, V, T, q);
+    double S = 0.0;
+    for (int j = 0; j < V; ++j) {
+      const double d = p[j] - q[j];
+      r[j] = d > 0.0 ? d : 0.0;
+      S += r[j];
+    }
+    if (S > 0.0 && S < kBand) flag |= ORACLE_FLAG_TINY_RESIDUAL;
+    chosen = S > 0.0 ? inverse_cdf(r, V, uK, &flag) : inverse_cdf(p, V, uK, &flag);
+  } else {
+    chosen = inverse_cdf(p, V, uK, &flag);
+  }
+  *n_out = n;
+  for (int i = 0; i < n; ++i) out[i] = x[i];
+  out[n] = chosen;
+  for (int i = n + 1; i <= K; ++i) out[i] = -1;
+  *flag_out = flag;
+  free(p); free(q); free(r); free(px); free(qx);
+  return 0;
+}
+
 /* One sequence in greedy mode ([BPD] sections 3.2 "Accept" and 3.5): g_i is
  * the argmax of target row i (lowest index on ties); n is the first i < K
  * with x_i != g_i, else K; emit x_0..x_{n-1} then g_n. */
@@ -326,6 +466,38 @@ int spec_oracle_verify(const void* target, const void* draft, const int32_t* tok
                              p_at, q_at, &f);
       if (flags) flags[b] = f;
     }
+    if (st < 0) nomem = 1;
+    else total |= st;
+  }
+  if (status) *status = total;
+  return nomem ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Speculative contrastive decoding over B sequences (scd_one); target and
+ * amateur are both [B, K+1, V]; alpha in [0, 1] is the plausibility cut of
+ * the contrastive head.  Outputs and status as spec_oracle_verify. */
+int spec_oracle_scd_verify(const void* target, const void* amateur, const int32_t* tokens,
+                           const float* uniforms, int B, int K, int V, int dtype,
+                           double temperature, double alpha, int32_t* accepted_len,
+                           int32_t* out_tokens, double* p_at, double* q_at, uint32_t* flags,
+                           int32_t* status) {
+  if (B < 0 || K < 0 || V < 1) return ORACLE_ERR_INVALID_ARG;
+  if (dtype != ORACLE_DTYPE_F32 && dtype != ORACLE_DTYPE_BF16) return ORACLE_ERR_INVALID_ARG;
+  if (!(temperature > 0.0) || isinf(temperature)) return ORACLE_ERR_INVALID_ARG;
+  if (!(alpha >= 0.0 && alpha <= 1.0)) return ORACLE_ERR_INVALID_ARG;
+  if (B == 0) { if (status) *status = 0; return ORACLE_OK; }
+  if (!target || !amateur || (K > 0 && !tokens) || !uniforms || !accepted_len || !out_tokens)
+    return ORACLE_ERR_INVALID_ARG;
+  const double L = alpha > 0.0 ? temperature * log(alpha) : -INFINITY;
+  int total = 0, nomem = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : total) reduction(| : nomem)
+  for (long long bb = 0; bb < (long long)B; ++bb) {
+    const size_t b = (size_t)bb;
+    uint32_t f = 0;
+    const int st = scd_one(target, amateur, tokens ? tokens + b * (size_t)K : NULL,
+                           uniforms + b * (size_t)(K + 1), K, V, dtype, temperature, L, b,
+                           &accepted_len[b], out_tokens + b * (size_t)(K + 1), p_at, q_at, &f);
+    if (flags) flags[b] = f;
     if (st < 0) nomem = 1;
     else total |= st;
   }

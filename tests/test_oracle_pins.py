@@ -683,3 +683,99 @@ def test_rejection_cut_data_errors_and_shapes():
         oracle.rejection_cut_ref(np.zeros((2, 0), np.float32), 0.5)
     empty = oracle.rejection_cut_ref(np.zeros((0, 5), np.float32), 0.5)
     assert empty["status"] == 0 and empty["n_accepted"].size == 0
+
+
+# --------------------------------------------------------------------------
+# Speculative contrastive decoding ("논문 리뷰 [Speculative Contrastive
+# Decoding]", section Speculative Contrastive Decoding): speculative sampling
+# against the contrastive target P_n of expert and amateur, bonus from P_n.
+# The page lost P_n's formula; the oracle reads it as contrastive decoding's
+# log p_e - log p_a over the plausible head {p_e >= alpha max p_e}.  That
+# formula stays unpinned by the pages; the pins below fix its two limits and
+# the exactness of the verify step against it.
+# --------------------------------------------------------------------------
+def _scd_inputs(B, K, V, seed, T=1.0, amateur_zero=False):
+    rng = np.random.default_rng(seed)
+    t = (rng.standard_normal((B, K + 1, V)) * 3).astype(np.float32)
+    t[:, :, 1] = -np.inf  # a masked token
+    a = np.zeros_like(t) if amateur_zero else (t + rng.standard_normal(t.shape)).astype(np.float32)
+    q = np.exp((a[:, :K] - a[:, :K].max(-1, keepdims=True)) / T)
+    q /= q.sum(-1, keepdims=True)
+    x = np.array([[rng.choice(V, p=q[b, i]) for i in range(K)] for b in range(B)], np.int32).reshape(B, K)
+    u = rng.random((B, K + 1), dtype=np.float32)
+    return t, a, x, u
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_scd_without_head_cut_and_a_flat_amateur_is_plain_speculative_sampling(T):
+    """alpha = 0 keeps every finite token and a flat amateur shifts every
+    contrast by a constant, so P_n = softmax(t / T) and q is uniform: the
+    outputs are those of the plain verify with all-zero draft logits."""
+    B, K, V = 64, 4, 50
+    t, a, x, u = _scd_inputs(B, K, V, 3, T, amateur_zero=True)
+    scd = oracle.scd_verify_ref(t, a, x, u, T, alpha=0.0, want_debug=True)
+    plain = oracle.verify_ref(t, np.zeros((B, K, V), np.float32), x, u, T, want_debug=True)
+    for k in ("accepted_len", "out_tokens", "p_at", "q_at", "flags"):
+        np.testing.assert_array_equal(scd[k], plain[k], err_msg=k)
+    assert scd["status"] == plain["status"] == 0
+
+
+def test_scd_with_the_tightest_head_is_greedy_verification():
+    """alpha = 1 leaves only the expert's argmax in the head, so P_n is a point
+    mass there: every draft token that is not the argmax is rejected and
+    replaced by it, which is Blockwise Parallel Decoding's greedy rule."""
+    B, K, V = 200, 5, 40
+    t, a, x, u = _scd_inputs(B, K, V, 4)
+    g = t.argmax(-1)
+    agree = np.random.default_rng(5).random((B, K)) < 0.6
+    x = np.where(agree, g[:, :K], x).astype(np.int32)
+    scd = oracle.scd_verify_ref(t, a, x, u, 1.0, alpha=1.0)
+    greedy = oracle.verify_ref(t, None, x, None, mode=oracle.MODE_GREEDY)
+    np.testing.assert_array_equal(scd["accepted_len"], greedy["accepted_len"])
+    np.testing.assert_array_equal(scd["out_tokens"], greedy["out_tokens"])
+    assert 0 < scd["accepted_len"].mean() < K
+
+
+def test_scd_emitted_token_follows_the_contrastive_target():
+    """The first emitted token is distributed as P_n at position 0, whatever
+    the amateur proposes (the exactness of speculative sampling with target
+    P_n); tokens outside the plausible head never appear."""
+    V, K, T, alpha, n = 8, 2, 0.9, 0.2, 200000
+    rng = np.random.default_rng(11)
+    t1 = (rng.standard_normal((K + 1, V)) * 1.5).astype(np.float32)
+    a1 = (rng.standard_normal((K + 1, V)) * 1.5).astype(np.float32)
+    td, ad = t1.astype(np.float64), a1.astype(np.float64)
+    head = td[0] >= td[0].max() + T * np.log(alpha)
+    pn = np.where(head, np.exp((td[0] - ad[0]) / T), 0.0)
+    pn /= pn.sum()
+    assert 0 < (~head).sum() < V
+    q = np.exp(ad[:K] / T)
+    q /= q.sum(-1, keepdims=True)
+    x = np.stack([rng.choice(V, size=n, p=q[i]) for i in range(K)], 1).astype(np.int32)
+    u = rng.random((n, K + 1), dtype=np.float32)
+    res = oracle.scd_verify_ref(np.broadcast_to(t1, (n, K + 1, V)), np.broadcast_to(a1, (n, K + 1, V)),
+                                x, u, T, alpha)
+    first = res["out_tokens"][:, 0]
+    counts = np.bincount(first, minlength=V)
+    assert counts[~head].sum() == 0
+    _, pval = stats.chisquare(counts[head], n * pn[head])
+    assert pval > 1e-3, pval
+
+
+def test_scd_data_errors_and_arguments():
+    B, K, V = 4, 2, 16
+    t, a, x, u = _scd_inputs(B, K, V, 6)
+    a[1, 0, 5] = np.nan
+    top = t[2, 1].argmax()
+    a[2, 1, top] = -np.inf          # an unbounded contrast inside the head
+    low = int(np.argsort(t[3, 0])[2])
+    a[3, 0, low] = -np.inf          # outside the head (alpha = 0.5): harmless if t is low enough
+    res = oracle.scd_verify_ref(t, a, x, u, 1.0, alpha=0.5)
+    assert res["status"] == oracle.DATA_LOGIT
+    assert res["accepted_len"][1] == -1 and res["accepted_len"][2] == -1
+    assert res["accepted_len"][0] >= 0
+    head3 = t[3, 0, low] >= t[3, 0].max() + np.log(0.5)
+    assert (res["accepted_len"][3] >= 0) == (not head3)
+    for bad in (-0.1, 1.5, float("nan")):
+        with pytest.raises(ValueError):
+            oracle.scd_verify_ref(t, a, x, u, 1.0, alpha=bad)
