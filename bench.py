@@ -387,9 +387,63 @@ def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
         if inp.mode == W.MODE_SAMPLE and inp.K > 0:
             table[name + "+early_exit"] = early_exit_line(binding, inp, steps, dev, l2, peak, sec)
             table[name + "+draft_sample"] = draft_sample_line(binding, inp, steps, dev, l2, peak)
+    for name, spec in W.SCD_WORKLOADS.items():
+        table[name] = scd_line(binding, spec, steps, dev, l2, peak)
     for name, spec in W.REJECTION_WORKLOADS.items():
         table[name] = rejection_cut_line(binding, spec, steps, dev, l2, peak)
     return table
+
+
+def scd_line(binding, spec, steps, dev, l2, peak):
+    """Speculative contrastive decoding's verify step (bytes: every expert
+    and amateur row read once, the tokens, the uniforms and the outputs),
+    graph-replayed over rotating input copies > 2x L2 like the rest."""
+    import torch
+    from draft_verify_acceptance_gb300 import workloads as W
+    spec = dict(spec)
+    alpha = spec.pop("alpha")
+    inp = W.make_scd_inputs(seed=0, **spec)
+    B, K, V = inp.B, inp.K, inp.V
+    es = inp.target.element_size()
+    nbytes = 2 * B * (K + 1) * V * es + B * K * 4 + B * (K + 1) * 4 + B * 4 + B * (K + 1) * 4
+    R = min(64, max(2, math.ceil(2 * l2 / max(nbytes, 1)) + 1))
+    copies = [tuple(t.to(dev) for t in (inp.target, inp.draft, inp.tokens, inp.uniforms))
+              for _ in range(R)]
+    dt = binding.DTYPE_BF16 if inp.target.dtype == torch.bfloat16 else binding.DTYPE_F32
+    ws = torch.zeros(binding.workspace_size(B, K, V, dt, binding.MODE_SAMPLE), dtype=torch.uint8,
+                     device=dev)
+    out = (torch.empty(B, dtype=torch.int32, device=dev),
+           torch.empty((B, K + 1), dtype=torch.int32, device=dev))
+    stream = torch.cuda.Stream(dev)
+
+    def launch(k):
+        c = copies[k % R]
+        binding.verify_scd(c[0], c[1], c[2], c[3], inp.temperature, alpha, stream=stream,
+                           workspace=ws, out=out)
+
+    with torch.cuda.stream(stream):
+        for r in range(3):
+            launch(r)
+        stream.synchronize()
+        n = min(steps, 1000)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n):
+                launch(k)
+        g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    mean_n = float(out[0].float().mean().item())
+    del g, copies
+    torch.cuda.empty_cache()
+    return {"us_per_step": sec * 1e6, "positions_per_s": B * K / sec, "bytes": nbytes,
+            "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
+            "kernel": "scd_row_kernel", "mean_accepted_len": mean_n}
 
 
 def rejection_cut_line(binding, spec, steps, dev, l2, peak):

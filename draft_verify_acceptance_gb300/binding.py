@@ -39,7 +39,7 @@ FLAG_RATIO = 1
 FLAG_CDF = 2
 
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_status_string",
-           "spec_verify_static", "spec_draft_sample", "spec_rejection_cut")
+           "spec_verify_static", "spec_draft_sample", "spec_rejection_cut", "spec_verify_scd")
 
 
 class SpecVerifyError(RuntimeError):
@@ -65,6 +65,9 @@ def _load():
     lib.spec_verify_static.argtypes = [P, P, P, P, I, I, I, I, F, I, P, P, P]
     lib.spec_draft_sample.restype = I
     lib.spec_draft_sample.argtypes = [P, P, I, I, I, F, P, P, P, Z, P, P]
+    lib.spec_verify_scd.restype = I
+    lib.spec_verify_scd.argtypes = [P, P, P, P, I, I, I, I, F, ctypes.c_double, P, P, P, Z, P,
+                                    P, P, P, P]
     lib.spec_rejection_cut.restype = I
     lib.spec_rejection_cut.argtypes = [P, I, I, ctypes.c_double, P, P, P, P, P]
     lib.spec_status_string.restype = ctypes.c_char_p
@@ -246,6 +249,58 @@ def draft_sample(logits, uniforms, temperature=1.0, *, stream=None, workspace=No
     if rc != OK:
         raise SpecVerifyError(rc, "spec_draft_sample")
     return (tokens, q_at, status) if debug else (tokens, q_at)
+
+
+def verify_scd(target, amateur, tokens, uniforms, temperature=1.0, alpha=0.1, *, stream=None,
+               workspace=None, out=None, debug=False):
+    """Speculative contrastive decoding's verify step on the GPU: target and
+    amateur [B, K+1, V] (float32 or bfloat16, CUDA, 16-byte aligned rows),
+    tokens [B, K] int32 (drawn from the amateur), uniforms [B, K+1] float32,
+    alpha the plausibility cut of the contrastive head.  Returns
+    (accepted_len, out_tokens), or with ``debug`` a dict that adds p_at
+    (P_n(x_i)), q_at, flags and status; queued on ``stream``."""
+    if target is None or target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    device = target.device
+    B, K1, V = target.shape
+    K = K1 - 1
+    _check(target, "target", (torch.float32, torch.bfloat16), (B, K1, V), device)
+    _check(amateur, "amateur", (target.dtype,), (B, K1, V), device)
+    if K > 0:
+        _check(tokens, "tokens", (torch.int32,), (B, K), device)
+    _check(uniforms, "uniforms", (torch.float32,), (B, K1), device)
+    dt = DTYPE_BF16 if target.dtype == torch.bfloat16 else DTYPE_F32
+    stream = stream or torch.cuda.current_stream(device)
+    if out is not None:
+        acc, res = out
+        _check(acc, "accepted_len", (torch.int32,), (B,), device)
+        _check(res, "out_tokens", (torch.int32,), (B, K1), device)
+    else:
+        acc = torch.empty(B, dtype=torch.int32, device=device)
+        res = torch.empty((B, K1), dtype=torch.int32, device=device)
+    need = workspace_size(B, K, V, dt, MODE_SAMPLE)
+    if need == 0 and B > 0:
+        raise SpecVerifyError(ERR_UNSUPPORTED if K > MAX_K or V > MAX_V else ERR_INVALID_ARG,
+                              "workspace size")
+    ws = workspace if workspace is not None else workspace_for(device, stream, need)
+    ex = None
+    if debug:
+        ex = dict(p_at=torch.zeros((B, K), dtype=torch.float32, device=device),
+                  q_at=torch.zeros((B, K), dtype=torch.float32, device=device),
+                  flags=torch.zeros(B, dtype=torch.int32, device=device),
+                  status=torch.zeros(1, dtype=torch.int32, device=device))
+    with torch.cuda.device(device):
+        rc = _lib.spec_verify_scd(
+            _ptr(target), _ptr(amateur), _ptr(tokens if K > 0 else None), _ptr(uniforms), B, K, V,
+            dt, float(temperature), float(alpha), _ptr(acc), _ptr(res), _ptr(ws), ws.numel(),
+            ctypes.c_void_p(stream.cuda_stream), _ptr(ex and ex["p_at"]), _ptr(ex and ex["q_at"]),
+            _ptr(ex and ex["flags"]), _ptr(ex and ex["status"]))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_verify_scd")
+    if debug:
+        ex.update(accepted_len=acc, out_tokens=res)
+        return ex
+    return acc, res
 
 
 def rejection_cut(scores, alpha, *, stream=None, out=None, debug=False):

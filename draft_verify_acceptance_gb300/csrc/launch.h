@@ -81,6 +81,13 @@ cudaError_t launch_row_sample(const void* logits, const float* uniforms, int R, 
                               float scale, int32_t* tokens, float* q_at, int32_t* status, int C,
                               cudaStream_t stream);
 
+// Speculative contrastive decoding: one cluster of C CTAs per row pair
+// (target, amateur), both staged in shared memory; L = T ln(alpha).
+int scd_cluster(long long nvec);
+cudaError_t scd_prepare();
+cudaError_t launch_scd(const VerifyArgs& a, const void* amateur, double L, int C,
+                       cudaStream_t stream);
+
 // Speculative Rejection's cut: r_cut and the kept indices per prompt
 // (j, g from alpha (N - 1) on the host).
 cudaError_t launch_rejection_cut(const float* scores, int G, int N, int j, double g,

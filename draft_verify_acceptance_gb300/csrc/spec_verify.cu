@@ -32,6 +32,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     if (e == cudaSuccess) e = sample_fused_prepare();
     if (e == cudaSuccess) e = sample_2p_prepare(&d);
     if (e == cudaSuccess) e = row_sample_prepare();
+    if (e == cudaSuccess) e = scd_prepare();
     g_info[device] = d;
     g_err[device] = e;
   });
@@ -204,6 +205,71 @@ spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
   const cudaError_t e = specv::launch_sample(a, info, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify_scd(const void* target_logits, const void* amateur_logits,
+                              const int32_t* draft_tokens, const float* uniforms, int B, int K,
+                              int V, int dtype, float temperature, double alpha,
+                              int32_t* accepted_len, int32_t* out_tokens, void* workspace,
+                              size_t workspace_bytes, spec_stream_t stream, float* p_at_draft,
+                              float* q_at_draft, uint32_t* flags, int32_t* device_status) {
+  if (B < 0 || K < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.f && std::isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
+  if (!(alpha >= 0.0 && alpha <= 1.0)) return SPEC_ERR_INVALID_ARG;
+  if (K > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  const int esz = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  if (!target_logits || !aligned(target_logits, esz)) return SPEC_ERR_INVALID_ARG;
+  if (!amateur_logits || !aligned(amateur_logits, esz)) return SPEC_ERR_INVALID_ARG;
+  if (K > 0 && (!draft_tokens || !aligned(draft_tokens, 4))) return SPEC_ERR_INVALID_ARG;
+  if (!uniforms || !aligned(uniforms, 4)) return SPEC_ERR_INVALID_ARG;
+  if (!accepted_len || !aligned(accepted_len, 4)) return SPEC_ERR_INVALID_ARG;
+  if (!out_tokens || !aligned(out_tokens, 4)) return SPEC_ERR_INVALID_ARG;
+  if ((p_at_draft && !aligned(p_at_draft, 4)) || (q_at_draft && !aligned(q_at_draft, 4)) ||
+      (flags && !aligned(flags, 4)) || (device_status && !aligned(device_status, 4)))
+    return SPEC_ERR_INVALID_ARG;
+  const size_t need = specv::workspace_bytes(B, K, V, esz);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return SPEC_ERR_INVALID_ARG;
+  const long long rowbytes = static_cast<long long>(V) * esz;
+  if (rowbytes % 16 != 0 || !aligned(target_logits, 16) || !aligned(amateur_logits, 16))
+    return SPEC_ERR_UNSUPPORTED;
+  const int C = specv::scd_cluster(rowbytes / 16);
+  if (C == 0) return SPEC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * (K + 1) * C > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  specv::DeviceInfo info;
+  if (specv::device_info(dev, &info) != cudaSuccess) return SPEC_ERR_CUDA;
+
+  specv::VerifyArgs a;
+  a.target = target_logits;
+  a.draft = nullptr;
+  a.tokens = draft_tokens;
+  a.uniforms = uniforms;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.bf16 = dtype == SPEC_DTYPE_BF16;
+  a.vec = true;
+  a.scale = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.accepted_len = accepted_len;
+  a.out_tokens = out_tokens;
+  a.p_at = p_at_draft;
+  a.q_at = q_at_draft;
+  a.flags = flags;
+  a.status = device_status;
+  const specv::WorkspaceLayout lay = specv::workspace_layout(B, K, V, esz);
+  a.seq = reinterpret_cast<specv::SeqState*>(static_cast<char*>(workspace) + lay.seq);
+  a.slots = static_cast<char*>(workspace) + lay.units;
+  a.partials = static_cast<char*>(workspace) + lay.units;
+  a.ctl = static_cast<char*>(workspace) + lay.ctl;
+  // the head's log-threshold T ln(alpha), in double (alpha = 0: no cut)
+  const double L = alpha > 0.0 ? static_cast<double>(temperature) * std::log(alpha) : -INFINITY;
+  const cudaError_t e =
+      specv::launch_scd(a, amateur_logits, L, C, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -1,0 +1,408 @@
+// verify_scd.cu -- speculative contrastive decoding's verify step on sm_103a:
+// speculative sampling against the contrastive target P_n of an expert
+// (target) and an amateur (drafter), with the bonus token drawn from P_n.
+//
+// Sources (page title, section):
+//   "논문 리뷰 [Speculative Contrastive Decoding]", Speculative Contrastive
+//     Decoding: the amateur drafts gamma tokens; the expert checks them
+//     against the contrastive-decoding distribution P_n instead of its own;
+//     when all are accepted the extra token comes from P_n too.
+//   "推测性拒绝采样", 技术原理与步骤 steps 3-4 and 关键保证: the accept test,
+//     the first rejection, and the residual law normalize(max(0, P - q)) that
+//     keeps the output distributed as the target (here P_n).
+// The page lost P_n's formula; this file reads it as contrastive decoding's
+//   P_n(j) ~ exp((t_j - a_j) / T)  on the head { t_j >= max t + T ln alpha }
+// (p_e(j) >= alpha * max p_e, p_e = softmax(t / T)), 0 elsewhere.  The head
+// test is taken exactly: thr = the double M + T ln alpha rounded up to fp32,
+// and t_j >= thr in fp32 (thr is the smallest float >= M + T ln alpha).
+//
+// Design: one cluster of C CTAs per row (b, i), i = 0..K.  Each CTA copies
+// its slice of the target row and of the amateur row into shared memory once
+// (bulk copies), so both rows cross HBM once.  From shared memory: (1) the
+// target row's maximum, exchanged over the cluster (DSMEM), which fixes the
+// head; (2) the online normalisers of the contrast (t - a) * s on the head
+// and, at draft positions, of the amateur a * s, merged in rank order; rank
+// 0 then runs the accept test of x_i and decides whether the row needs a
+// draw (a rejected draft position with no earlier rejection, or the bonus
+// row); (3) the fixed-point masses of max(0, P_n - q) (or of P_n) per vector,
+// summed per (tile, warp) and per slice, exchanged over the cluster; (4) the
+// CTA holding the draw's threshold finds the token and stores it as the
+// row's candidate.  The rows of a sequence meet through its arrival counter;
+// the last one writes the outputs (the same protocol as the streaming
+// sampler).  Every wait is bounded.
+#include <cooperative_groups.h>
+
+#include <cfloat>
+#include <climits>
+#include <cmath>
+
+#include "../../include/spec_verify.h"
+#include "device_common.cuh"
+#include "launch.h"
+#include "sample_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace specv {
+namespace {
+
+constexpr int kThreadsS = 256;
+constexpr int kWarpsS = kThreadsS / 32;
+constexpr int kMaxCS = 8;
+constexpr long long kPairBytes2 = 96 * 1024;   // both slices, two CTAs per SM
+constexpr long long kPairBytes1 = 200 * 1024;  // both slices, one CTA per SM
+constexpr int kCopyVecS = 2048;                // vectors per bulk copy (32 KiB)
+
+struct __align__(16) Norm4 {
+  float msc, zc, msa, za;
+};
+
+// Online normaliser of VEC values relative to a scaled offset: terms
+// 2^(x * s - ms).  -inf values add nothing.
+template <int VEC>
+__device__ __forceinline__ void acc_floats(RowAcc& A, const float (&x)[VEC], float s) {
+  float mx = x[0];
+#pragma unroll
+  for (int k = 1; k < VEC; ++k) mx = fmaxf(mx, x[k]);
+  const float nm = fmaxf(A.ms, mx * s);
+  if (nm == -INFINITY) return;
+  const float f = (A.ms == nm) ? 1.f : ex2(A.ms - nm);
+  float e = 0.f;
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) e += ex2(__fmaf_rn(x[k], s, -nm));
+  A.z = fmaf(A.z, f, e);
+  A.ms = nm;
+}
+
+// Contrast of one element: t - a on the head, -inf elsewhere.
+__device__ __forceinline__ float contrast(float t, float a, float thr) {
+  return (t >= thr && t > -INFINITY) ? __fsub_rn(t, a) : -INFINITY;
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kThreadsS, 2)
+scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, double L) {
+  constexpr int VEC = Staged<E>::kVec;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int lgC = __ffs(C) - 1;  // C is a power of two
+  const int row = static_cast<int>(blockIdx.x >> lgC);
+  const int K = a.K, K1 = K + 1;
+  const int b = row / K1, i = row - b * K1;
+  const bool has_draft = i < K;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long v0 = (nvec * rank) >> lgC;
+  const int nv = static_cast<int>(((nvec * (rank + 1)) >> lgC) - v0);
+  const int ntl = (nv + kThreadsS - 1) / kThreadsS;
+  const long long nvs = (nvec + C - 1) >> lgC;
+
+  extern __shared__ __align__(128) uint4 smem[];
+  uint4* tsl = smem;                        // [nvs] target slice
+  uint4* asl = smem + nvs;                  // [nvs] amateur slice
+  unsigned long long* tws = reinterpret_cast<unsigned long long*>(smem + 2 * nvs);
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ float s_wmax[kWarpsS];
+  __shared__ float s_pmax[kMaxCS];          // pushed by each rank
+  __shared__ Norm4 s_warp[kWarpsS];
+  __shared__ Norm4 s_part[kMaxCS];          // pushed by each rank
+  __shared__ unsigned long long s_mass[kMaxCS];
+  __shared__ int s_need, s_bad;
+
+  const size_t roff = static_cast<size_t>(row) * nvec;
+  const uint4* tsrc = static_cast<const uint4*>(a.target) + roff + v0;
+  const uint4* asrc = static_cast<const uint4*>(amateur) + roff + v0;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    s_bad = 0;
+  }
+  __syncthreads();
+  if (tid == 0 && nv > 0) {
+    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nv) * 32u);
+    for (int c0 = 0; c0 < nv; c0 += kCopyVecS) {
+      const uint32_t len = static_cast<uint32_t>(min(kCopyVecS, nv - c0)) * 16u;
+      bulk_load(tsl + c0, tsrc + c0, len, &bar);
+      bulk_load(asl + c0, asrc + c0, len, &bar);
+    }
+  }
+  cluster_arrive_relaxed();  // matched before the first DSMEM push
+  bool ok = true;
+  if (nv > 0 && !mbar_wait_sleep(&bar, 0u)) ok = false;
+
+  // ---- (1) the target row's maximum ---------------------------------------
+  float mx = -INFINITY;
+  bool bad = false;
+  for (int v = tid; v < nv; v += kThreadsS) {
+    float xt[VEC], xa[VEC];
+    Staged<E>::unpack(tsl[v], xt);
+    Staged<E>::unpack(asl[v], xa);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      mx = fmaxf(mx, xt[k]);
+      bad |= (!(xt[k] <= FLT_MAX) && !(xt[k] == -INFINITY)) ||
+             (!(xa[k] <= FLT_MAX) && !(xa[k] == -INFINITY));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) s_wmax[warp] = mx;
+  if (__syncthreads_or(bad) && tid == 0) s_bad = 1;
+  cluster_wait();  // every CTA of the cluster has started
+  if (warp == 0) {
+    float m = lane < kWarpsS ? s_wmax[lane] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane < C) *cluster.map_shared_rank(&s_pmax[rank], lane) = m;
+  }
+  cluster.sync();
+  float M = -INFINITY;
+  for (int r = 0; r < C; ++r) M = fmaxf(M, s_pmax[r]);
+  const float thr = __double2float_ru(__dadd_rn(static_cast<double>(M), L));
+
+  // ---- (2) normalisers of the contrast on the head and of the amateur -----
+  RowAcc Ac{-INFINITY, 0.f}, Aa{-INFINITY, 0.f};
+  bool unbounded = false;  // a head token the amateur gives no mass
+  for (int v = tid; v < nv; v += kThreadsS) {
+    float xt[VEC], xa[VEC], xc[VEC];
+    Staged<E>::unpack(tsl[v], xt);
+    Staged<E>::unpack(asl[v], xa);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      xc[k] = contrast(xt[k], xa[k], thr);
+      unbounded |= xc[k] == INFINITY;
+    }
+    acc_floats<VEC>(Ac, xc, s);
+    if (has_draft) acc_floats<VEC>(Aa, xa, s);
+  }
+  warp_merge_scaled(Ac.ms, Ac.z);
+  warp_merge_scaled(Aa.ms, Aa.z);
+  if (lane == 0) s_warp[warp] = Norm4{Ac.ms, Ac.z, Aa.ms, Aa.z};
+  if (__syncthreads_or(unbounded) && tid == 0) s_bad = 1;
+  if (warp == 0) {
+    Norm4 m = lane < kWarpsS ? s_warp[lane] : Norm4{-INFINITY, 0.f, -INFINITY, 0.f};
+    warp_merge_scaled(m.msc, m.zc);
+    warp_merge_scaled(m.msa, m.za);
+    if (lane < C) *cluster.map_shared_rank(&s_part[rank], lane) = m;
+  }
+  cluster.sync();
+  float MSc = -INFINITY, Zc = 0.f, MSa = -INFINITY, Za = 0.f;
+  for (int r = 0; r < C; ++r) {  // rank order: the same bits in every CTA
+    merge_scaled(MSc, Zc, s_part[r].msc, s_part[r].zc);
+    merge_scaled(MSa, Za, s_part[r].msa, s_part[r].za);
+  }
+  const bool norm_ok = isfinite(MSc) && isfinite(Zc) && Zc > 0.f &&
+                       (!has_draft || (isfinite(MSa) && isfinite(Za) && Za > 0.f));
+  const float invZc = norm_ok ? 1.f / Zc : 0.f;
+  const float invZa = (norm_ok && has_draft) ? 1.f / Za : 0.f;
+  const float uK = a.uniforms[static_cast<size_t>(b) * K1 + K];
+
+  // ---- accept test and whether this row needs a draw (rank 0) -------------
+  if (rank == 0 && tid == 0) {
+    SeqState* st = a.seq + b;
+    int err = 0;
+    if (!norm_ok) err |= kDataNonfiniteLogit;
+    bool need = true;
+    if (has_draft) {
+      const int xr = a.tokens[static_cast<size_t>(b) * K + i];
+      const int x = min(max(xr, 0), a.V - 1);
+      const float ui = a.uniforms[static_cast<size_t>(b) * K1 + i];
+      const void* trow = static_cast<const char*>(a.target) + roff * 16;
+      const void* arow = static_cast<const char*>(amateur) + roff * 16;
+      const float tx = load_one<E>(trow, x), ax = load_one<E>(arow, x);
+      const float cx = contrast(tx, ax, thr);
+      const float px = __fmul_rn(ex2(__fmaf_rn(cx, s, -MSc)), invZc);
+      const float qx = __fmul_rn(ex2(__fmaf_rn(ax, s, -MSa)), invZa);
+      const bool accept = ui * qx < px;
+      if (a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
+      if (a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
+      if (xr != x) err |= kDataTokenRange;
+      if (!(ui >= 0.f && ui < 1.f)) err |= kDataUniformRange;
+      if (qx > 0.f && fabsf(ui - fminf(1.f, px / qx)) < kBandF)
+        atomicOr(&st->near_mask, 1ull << i);
+      if (!accept) atomicOr(&st->reject_mask, 1ull << i);
+      need = !accept;
+    } else if (!(uK >= 0.f && uK < 1.f)) {
+      err |= kDataUniformRange;
+    }
+    if (err && a.status) atomicOr(a.status, err);
+    __threadfence();
+    if (need) {
+      const unsigned long long m = *reinterpret_cast<volatile unsigned long long*>(&st->reject_mask);
+      const unsigned long long earlier = (i >= 64) ? ~0ull : ((1ull << i) - 1ull);
+      if (m & earlier) need = false;  // an earlier position already rejected
+    }
+    for (int r = 0; r < C; ++r) *cluster.map_shared_rank(&s_need, r) = need ? 1 : 0;
+  }
+  // any CTA that saw a bad element or a lost copy reports it
+  if (tid == 0 && (s_bad || !ok) && a.status)
+    atomicOr(a.status, (s_bad ? kDataNonfiniteLogit : 0) | (ok ? 0 : kWaitTimeout));
+  cluster.sync();
+  if (!s_need) {
+    if (rank == 0 && warp == 0) warp_arrive_and_finalize(a, b);
+    return;
+  }
+
+  // ---- (3) fixed-point masses of max(0, P_n - q) (or P_n) -----------------
+  bool residual = has_draft;
+  unsigned long long S = 0;
+  for (int rnd = 0; rnd < 2; ++rnd) {
+    for (int k = 0; k < ntl; ++k) {
+      const int v = k * kThreadsS + tid;
+      float xc[VEC], xa[VEC], r[VEC];
+      if (v < nv) {
+        float xt[VEC];
+        Staged<E>::unpack(tsl[v], xt);
+        Staged<E>::unpack(asl[v], xa);
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) xc[q] = contrast(xt[q], xa[q], thr);
+      } else {
+#pragma unroll
+        for (int q = 0; q < VEC; ++q) xc[q] = xa[q] = -INFINITY;
+      }
+      const unsigned long long w = warp_sum_mass(
+          vec_weight_scaled<VEC>(xc, xa, MSc, invZc, MSa, invZa, s, residual, r));
+      if (lane == 0) tws[k * kWarpsS + warp] = w;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long t = 0;
+      for (int k = lane; k < ntl * kWarpsS; k += 32) t += tws[k];
+      t = warp_sum_u64(t);
+      if (lane < C) *cluster.map_shared_rank(&s_mass[rank], lane) = t;
+    }
+    cluster.sync();
+    S = 0;
+    for (int r = 0; r < C; ++r) S += s_mass[r];
+    if (S != 0 || !residual) break;
+    residual = false;  // P_n == q at this row: the draw falls back to P_n
+    cluster.sync();    // every CTA has read s_mass before it is pushed again
+  }
+
+  // ---- (4) the crossing, in the CTA that holds it (warp 0) ----------------
+  const unsigned long long theta = draw_threshold(uK, S);
+  int cstar = C - 1;
+  unsigned long long off = 0;
+  for (int r = 0; r < C; ++r) {
+    if (off + s_mass[r] > theta) {
+      cstar = r;
+      break;
+    }
+    off += s_mass[r];
+  }
+  if (rank != cstar || warp != 0) return;
+  int32_t cand = 0;
+  if (S != 0 && ntl > 0) {
+    const unsigned long long tl = theta - off;
+    unsigned long long base = 0;
+    int kstar = ntl - 1;
+    for (int k0 = 0; k0 < ntl; k0 += 32) {
+      const int k = k0 + lane;
+      unsigned long long tt = 0;
+      if (k < ntl)
+        for (int w = 0; w < kWarpsS; ++w) tt += tws[k * kWarpsS + w];
+      const unsigned long long incl = warp_scan_u64(tt, lane);
+      const unsigned int hit = __ballot_sync(0xffffffffu, k < ntl && base + incl > tl);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        base += __shfl_sync(0xffffffffu, incl - tt, l);
+        kstar = k0 + l;
+        break;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    int wstar = kWarpsS - 1;
+    {
+      const unsigned long long m = lane < kWarpsS ? tws[kstar * kWarpsS + lane] : 0ull;
+      const unsigned long long incl = warp_scan_u64(m, lane);
+      const unsigned int hit = __ballot_sync(0xffffffffu, lane < kWarpsS && base + incl > tl);
+      if (hit) wstar = __ffs(hit) - 1;
+      base += __shfl_sync(0xffffffffu, incl - m, wstar);
+    }
+    const int v = kstar * kThreadsS + wstar * 32 + lane;
+    float xc[VEC], xa[VEC], r[VEC];
+    if (v < nv) {
+      float xt[VEC];
+      Staged<E>::unpack(tsl[v], xt);
+      Staged<E>::unpack(asl[v], xa);
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) xc[q] = contrast(xt[q], xa[q], thr);
+    } else {
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) xc[q] = xa[q] = -INFINITY;
+    }
+    const unsigned long long w =
+        vec_weight_scaled<VEC, true>(xc, xa, MSc, invZc, MSa, invZa, s, residual, r);
+    const unsigned long long incl = warp_scan_u64(w, lane);
+    const unsigned int hit = __ballot_sync(0xffffffffu, base + incl > tl);
+    const int lstar = hit ? __ffs(hit) - 1 : 31;
+    if (lane == lstar) {
+      const unsigned long long before = base + incl - w;
+      unsigned long long c_prev, c_cur;
+      const int mstar = pick_in_vector<VEC>(r, w, tl - before, c_prev, c_cur);
+      const long long t = (v0 + v) * VEC + mstar;
+      const int32_t tok = static_cast<int32_t>(t < a.V ? t : a.V - 1);
+      const bool near = near_step(theta, off + before + c_prev, off + before + c_cur, S);
+      cand = near ? static_cast<int32_t>(static_cast<uint32_t>(tok) | 0x80000000u) : tok;
+    }
+    cand = __shfl_sync(0xffffffffu, cand, lstar);
+  }
+  if (lane == 0) {
+    *candidate_slot(a, b, i) = cand;
+    __threadfence();
+  }
+  __syncwarp();
+  warp_arrive_and_finalize(a, b);
+}
+
+}  // namespace
+
+// Cluster size for row pairs of nvec vectors: the smallest C in {1, 2, 4, 8}
+// whose two slices fit kPairBytes2 (two CTAs per SM), else 8 if they fit
+// kPairBytes1; 0 when the rows are too long.
+int scd_cluster(long long nvec) {
+  for (int C = 1; C <= kMaxCS; C *= 2)
+    if (((nvec + C - 1) / C) * 32 <= kPairBytes2) return C;
+  if (((nvec + kMaxCS - 1) / kMaxCS) * 32 <= kPairBytes1) return kMaxCS;
+  return 0;
+}
+
+static size_t scd_smem(long long nvec, int C) {
+  const long long nvs = (nvec + C - 1) / C;
+  const long long ntl = (nvs + kThreadsS - 1) / kThreadsS;
+  return static_cast<size_t>(nvs * 32 + ntl * kWarpsS * 8);
+}
+
+cudaError_t scd_prepare() {
+  const int smem = static_cast<int>(kPairBytes1) + 8 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(scd_row_kernel<BF16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(scd_row_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+  return e;
+}
+
+cudaError_t launch_scd(const VerifyArgs& a, const void* amateur, double L, int C,
+                       cudaStream_t stream) {
+  const int esz = a.bf16 ? 2 : 4;
+  const long long nvec = static_cast<long long>(a.V) * esz / 16;
+  const long long grid = static_cast<long long>(a.B) * (a.K + 1) * C;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned int>(grid));
+  cfg.blockDim = dim3(kThreadsS);
+  cfg.dynamicSmemBytes = scd_smem(nvec, C);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.bf16 ? cudaLaunchKernelEx(&cfg, scd_row_kernel<BF16>, a, amateur, nvec, a.scale, L)
+                : cudaLaunchKernelEx(&cfg, scd_row_kernel<F32>, a, amateur, nvec, a.scale, L);
+}
+
+}  // namespace specv

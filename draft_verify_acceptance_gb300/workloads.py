@@ -124,6 +124,44 @@ WORKLOADS = {
 }
 
 
+def make_scd_inputs(B, K, V, *, dtype=torch.float32, temperature=1.0, target_std=3.0,
+                    zipf_s=0.0, amateur_noise=1.0, independent_amateur=False, seed=0,
+                    name=None) -> Inputs:
+    """Inputs of speculative contrastive decoding's verify step: the expert's
+    logits as make_inputs' target; the amateur's [B, K+1, V] logits (held in
+    ``draft``) = the expert's + amateur_noise * N(0,1) (stream 5), or an
+    independent target_std * N(0,1) draw; draft tokens drawn from
+    softmax(amateur[:, :K] / T) after the dtype cast (stream 6); uniforms as
+    make_inputs'."""
+    base = make_inputs(B, K, V, dtype=dtype, temperature=temperature, target_std=target_std,
+                       zipf_s=zipf_s, seed=seed, name=name)
+    g_a, g_x = _gen(seed, 5), _gen(seed, 6)
+    if independent_amateur:
+        a32 = torch.randn((B, K + 1, V), generator=g_a, dtype=torch.float32) * target_std
+    else:
+        a32 = base.target.float() + amateur_noise * torch.randn((B, K + 1, V), generator=g_a,
+                                                                dtype=torch.float32)
+    amateur = a32.to(dtype).contiguous()
+    if K > 0 and B > 0:
+        w = torch.softmax(amateur[:, :K].float().reshape(B * K, V) / temperature, dim=-1)
+        tokens = torch.multinomial(w, 1, generator=g_x).reshape(B, K)
+    else:
+        tokens = torch.zeros((B, K), dtype=torch.int64)
+    recipe = dict(target_std=target_std, zipf_s=zipf_s, amateur_noise=amateur_noise,
+                  independent_amateur=independent_amateur, seed=seed)
+    return Inputs(name or f"scd_B{B}_K{K}_V{V}", MODE_SAMPLE, B, K, V, float(temperature),
+                  base.target, amateur, tokens.to(torch.int32).contiguous(), base.uniforms, recipe)
+
+
+# Speculative contrastive decoding on the sampling workload's shapes: the
+# amateur is the expert plus N(0,1) noise, plausibility cut alpha = 0.1.
+SCD_WORKLOADS = {
+    "scd_bf16_B64_K5_V128256_T1.0_a0.1": dict(
+        B=64, K=5, V=128256, dtype=torch.bfloat16, temperature=1.0, target_std=4.0,
+        zipf_s=1.1, amateur_noise=1.0, alpha=0.1),
+}
+
+
 def make_scores(G: int, N: int, *, kind: str = "normal", seed: int = 0) -> torch.Tensor:
     """[G, N] float32 partial reward scores following the recipe above."""
     g = _gen(seed, 4)

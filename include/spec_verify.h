@@ -244,6 +244,53 @@ SPEC_API spec_status_t spec_draft_sample(const void* logits, const float* unifor
                                          spec_stream_t stream, int32_t* device_status);
 
 /*
+ * spec_verify_scd -- the verify step of speculative contrastive decoding
+ * ("논문 리뷰 [Speculative Contrastive Decoding]", section Speculative
+ * Contrastive Decoding): the amateur (the drafter) proposes x_0..x_{K-1};
+ * the expert (the target) checks them against the contrastive-decoding
+ * distribution P_n instead of its own p, and when all K are accepted the
+ * extra token is drawn from P_n as well.  The page lost P_n's formula; this
+ * library reads it as contrastive decoding's log p_e - log p_a on the
+ * plausible head:
+ *
+ *   head_i = { j : t[b,i,j] > -inf and p_e(j) >= alpha * max p_e },
+ *            p_e = softmax(t[b,i] / T), i.e. t_j >= max_j t + T ln(alpha)
+ *            (taken exactly: the double max + T ln(alpha), rounded up to fp32)
+ *   P_n,i(j) = exp((t[b,i,j] - a[b,i,j]) / T) / Z_i on head_i, 0 elsewhere
+ *   q_i = softmax(a[b,i] / T)  (the amateur's distribution x_i was drawn from)
+ *
+ * and otherwise follows spec_verify's sampling mode with p replaced by P_n:
+ * accept x_i iff u_i * q_i(x_i) < P_n,i(x_i); n = first rejection (K if
+ * none); at n < K the token is drawn from max(0, P_n,n - q_n) (P_n,n if that
+ * is zero everywhere), at n == K from P_n,K; same inverse CDF, same flags.
+ *
+ *   target_logits  [B, K+1, V] dtype, device: the expert's logits.
+ *   amateur_logits [B, K+1, V] dtype, device: the amateur's logits; row i < K
+ *                  is the distribution x_i was drawn from, row K enters only
+ *                  P_n,K (the amateur's step after x_{K-1}).
+ *   draft_tokens, uniforms, B, K, V, dtype, accepted_len, out_tokens,
+ *   workspace, stream, p_at_draft (P_n,i(x_i)), q_at_draft, flags,
+ *   device_status   as spec_verify_ex in sampling mode.  Temperature > 0.
+ *   alpha          in [0, 1]: 0 keeps every token with a finite target logit,
+ *                  1 only the target's argmax (then the result is greedy
+ *                  verification's).
+ * Rows must be 16-byte aligned (V times the element size a multiple of 16,
+ * both bases 16-byte aligned) and a row pair must fit eight CTAs' shared
+ * memory (V up to about 400k bf16 / 200k fp32): other calls return
+ * SPEC_ERR_UNSUPPORTED.  A NaN or +inf logit in either tensor, or a head
+ * token whose amateur logit is -inf (an unbounded contrast), sets
+ * SPEC_DATA_NONFINITE_LOGIT.  Asynchronous on `stream`.
+ */
+SPEC_API spec_status_t spec_verify_scd(const void* target_logits, const void* amateur_logits,
+                                       const int32_t* draft_tokens, const float* uniforms, int B,
+                                       int K, int V, int dtype, float temperature, double alpha,
+                                       int32_t* accepted_len, int32_t* out_tokens,
+                                       void* workspace, size_t workspace_bytes,
+                                       spec_stream_t stream, float* p_at_draft,
+                                       float* q_at_draft, uint32_t* flags,
+                                       int32_t* device_status);
+
+/*
  * spec_rejection_cut -- Speculative Rejection's cut (review "Speculative
  * Rejection", section 4.2 "算法", the speculative-rejection phase: the
  * partial responses are scored, r_cut is the alpha-quantile of the scores,

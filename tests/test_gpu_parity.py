@@ -461,3 +461,83 @@ def test_rejection_cut_empty_batch(lib):
     r, n, acc = lib.rejection_cut(torch.zeros((0, 10), device="cuda"), 0.5)
     torch.cuda.synchronize()
     assert r.numel() == 0 and n.numel() == 0 and acc.numel() == 0
+
+
+# --------------------------------------------------------------------------
+# Speculative contrastive decoding: the same bar as sampling mode, with the
+# oracle's contrastive target (the temperature passed to both sides as the
+# same fp32 value, so the head's threshold is the same double).
+# --------------------------------------------------------------------------
+SCD_CASES = [
+    # name, B, K, V, dtype, T, alpha, recipe  (cluster sizes 1, 2, 8 at two and one CTA per SM)
+    ("scd_f32_V1000", 16, 4, 1000, torch.float32, 1.0, 0.1, dict(target_std=3.0, amateur_noise=1.0)),
+    ("scd_bf16_V32000", 16, 4, 32000, torch.bfloat16, 0.7, 0.1, dict(target_std=3.0, amateur_noise=0.5)),
+    ("scd_bf16_V128256", 6, 5, 128256, torch.bfloat16, 1.0, 0.1,
+     dict(target_std=4.0, zipf_s=1.1, amateur_noise=1.0)),
+    ("scd_f32_V152064_low_accept", 3, 8, 152064, torch.float32, 0.8, 0.05,
+     dict(target_std=5.0, independent_amateur=True)),
+    ("scd_f32_alpha0", 8, 3, 5000, torch.float32, 1.0, 0.0, dict(target_std=3.0, amateur_noise=1.0)),
+    ("scd_f32_K0", 6, 0, 4096, torch.float32, 1.0, 0.2, dict(target_std=3.0)),
+    ("scd_bf16_V1024_T0.05", 16, 3, 1024, torch.bfloat16, 0.05, 0.3, dict(target_std=1.0, amateur_noise=0.1)),
+]
+
+
+def run_scd(lib, inp, alpha, T32):
+    res = lib.verify_scd(_dev(inp.target), _dev(inp.draft), _dev(inp.tokens), _dev(inp.uniforms),
+                         T32, alpha, debug=True)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in res.items()}
+
+
+def scd_oracle(inp, alpha, T32):
+    return oracle.scd_verify_ref(W.as_numpy_logits(inp.target), W.as_numpy_logits(inp.draft),
+                                 inp.tokens.numpy(), inp.uniforms.numpy(), T32, alpha,
+                                 want_debug=True)
+
+
+@pytest.mark.parametrize("name,B,K,V,dtype,T,alpha,recipe", SCD_CASES, ids=[c[0] for c in SCD_CASES])
+def test_scd_parity(lib, name, B, K, V, dtype, T, alpha, recipe):
+    inp = W.make_scd_inputs(B, K, V, dtype=dtype, temperature=T, name=name,
+                            seed=zlib.crc32(name.encode()) % 1000, **recipe)
+    T32 = float(np.float32(T))
+    assert_parity(run_scd(lib, inp, alpha, T32), scd_oracle(inp, alpha, T32), inp, name)
+
+
+def test_scd_full_size(lib):
+    """The benchmarked workload (64 sequences, K = 5, V = 128256 bf16)."""
+    spec = dict(W.SCD_WORKLOADS["scd_bf16_B64_K5_V128256_T1.0_a0.1"])
+    alpha = spec.pop("alpha")
+    inp = W.make_scd_inputs(seed=0, **spec)
+    T32 = float(np.float32(inp.temperature))
+    assert_parity(run_scd(lib, inp, alpha, T32), scd_oracle(inp, alpha, T32), inp, "scd full")
+
+
+def test_scd_tightest_head_is_greedy_on_gpu(lib):
+    inp = W.make_scd_inputs(32, 5, 32000, dtype=torch.bfloat16, target_std=4.0, amateur_noise=2.0,
+                            seed=9)
+    g = run_scd(lib, inp, 1.0, 1.0)
+    ref = oracle.verify_ref(W.as_numpy_logits(inp.target), None, inp.tokens.numpy(), None,
+                            mode=oracle.MODE_GREEDY)
+    np.testing.assert_array_equal(g["accepted_len"], ref["accepted_len"])
+    np.testing.assert_array_equal(g["out_tokens"], ref["out_tokens"])
+
+
+def test_scd_data_errors_and_workspace(lib):
+    inp = W.make_scd_inputs(6, 3, 2048, dtype=torch.float32, target_std=3.0, seed=12)
+    inp.draft[1, 2, 100] = float("nan")
+    top = int(inp.target[3, 1].argmax())
+    inp.draft[3, 1, top] = float("-inf")  # an unbounded contrast in the head
+    B, K, V = inp.B, inp.K, inp.V
+    ws = torch.zeros(lib.workspace_size(B, K, V, lib.DTYPE_F32, lib.MODE_SAMPLE), dtype=torch.uint8,
+                     device="cuda")
+    g = lib.verify_scd(_dev(inp.target), _dev(inp.draft), _dev(inp.tokens), _dev(inp.uniforms), 1.0,
+                       0.1, workspace=ws, debug=True)
+    torch.cuda.synchronize()
+    ref = oracle.scd_verify_ref(inp.target.numpy(), inp.draft.numpy(), inp.tokens.numpy(),
+                                inp.uniforms.numpy(), 1.0, 0.1, want_debug=True)
+    assert ref["status"] == oracle.DATA_LOGIT
+    assert int(g["status"].item()) == lib.DATA_NONFINITE_LOGIT
+    ok = (ref["accepted_len"] >= 0) & (ref["flags"] == 0)
+    assert ok.sum() >= 3
+    np.testing.assert_array_equal(g["accepted_len"].cpu().numpy()[ok], ref["accepted_len"][ok])
+    assert int(ws.count_nonzero().item()) == 0  # left zero-filled

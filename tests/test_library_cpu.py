@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(binding):
     names = _declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
                           "spec_status_string", "spec_verify_static", "spec_draft_sample",
-                          "spec_rejection_cut"}
+                          "spec_rejection_cut", "spec_verify_scd"}
     assert set(names) == set(binding.EXPORTS)
     lib = ctypes.CDLL(binding.LIB_PATH)
     for n in names:
@@ -197,3 +197,32 @@ def test_rejection_cut_host_checks(binding):
     assert call(s=ctypes.c_void_p((1 << 20) + 2)) == binding.ERR_INVALID_ARG
     assert call(st=ctypes.c_void_p((1 << 20) + 1)) == binding.ERR_INVALID_ARG
     assert call(G=0, N=0) == binding.OK
+
+
+def test_verify_scd_host_checks(binding):
+    """spec_verify_scd's argument errors return before any launch (fake,
+    never dereferenced pointers)."""
+    f = binding._lib.spec_verify_scd
+    fake = ctypes.c_void_p(1 << 20)
+    ws = binding.workspace_size(4, 3, 1024, binding.DTYPE_F32, binding.MODE_SAMPLE)
+    def call(B=4, K=3, V=1024, dtype=binding.DTYPE_F32, T=1.0, alpha=0.1, t=fake, a=fake, x=fake,
+             u=fake, nbytes=ws):
+        return f(t, a, x, u, B, K, V, dtype, T, alpha, fake, fake, fake, nbytes, None,
+                 None, None, None, None)
+    assert call(B=-1) == binding.ERR_INVALID_ARG
+    assert call(V=0) == binding.ERR_INVALID_ARG
+    assert call(dtype=5) == binding.ERR_INVALID_ARG
+    assert call(T=0.0) == binding.ERR_INVALID_ARG
+    for bad in (-0.5, 1.5, float("nan")):
+        assert call(alpha=bad) == binding.ERR_INVALID_ARG
+    assert call(a=None) == binding.ERR_INVALID_ARG
+    assert call(t=None) == binding.ERR_INVALID_ARG
+    assert call(x=None) == binding.ERR_INVALID_ARG
+    assert call(u=None) == binding.ERR_INVALID_ARG
+    assert call(nbytes=64) == binding.ERR_INVALID_ARG
+    assert call(K=binding.MAX_K + 1) == binding.ERR_UNSUPPORTED
+    wsu = binding.workspace_size(4, 3, 1001, binding.DTYPE_F32, binding.MODE_SAMPLE)
+    assert call(V=1001, nbytes=wsu) == binding.ERR_UNSUPPORTED  # rows not 16-byte multiples
+    wsl = binding.workspace_size(4, 3, 1 << 22, binding.DTYPE_F32, binding.MODE_SAMPLE)
+    assert call(V=1 << 22, nbytes=wsl) == binding.ERR_UNSUPPORTED  # a row pair beyond 8 CTAs
+    assert call(B=0) == binding.OK
