@@ -74,6 +74,39 @@ __device__ __forceinline__ void acc_floats(RowAcc& A, const float (&x)[VEC], flo
   A.ms = nm;
 }
 
+// Maximum that propagates NaN.
+__device__ __forceinline__ float nan_max(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Largest element of a 16-byte vector, NaN if it holds one.
+template <typename E>
+__device__ __forceinline__ float vec_max_nan(const uint4 w);
+template <>
+__device__ __forceinline__ float vec_max_nan<BF16>(const uint4 w) {
+  uint32_t m;
+  asm("{\n\t.reg .b32 t0, t1;\n\t"
+      "max.NaN.bf16x2 t0, %1, %2;\n\tmax.NaN.bf16x2 t1, %3, %4;\n\t"
+      "max.NaN.bf16x2 %0, t0, t1;\n\t}"
+      : "=r"(m) : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
+  return nan_max(bf16_lo(m), bf16_hi(m));
+}
+template <>
+__device__ __forceinline__ float vec_max_nan<F32>(const uint4 w) {
+  return nan_max(nan_max(__uint_as_float(w.x), __uint_as_float(w.y)),
+                 nan_max(__uint_as_float(w.z), __uint_as_float(w.w)));
+}
+
+// Largest element of a 16-byte vector (rows already known to hold no NaN).
+template <typename E>
+__device__ __forceinline__ float vec_max(const uint4 w) {
+  typename Staged<E>::Max m = Staged<E>::max_init();
+  Staged<E>::max_update(m, w);
+  return Staged<E>::max_value(m);
+}
+
 // Contrast of one element: t - a on the head, -inf elsewhere.
 __device__ __forceinline__ float contrast(float t, float a, float thr) {
   return (t >= thr && t > -INFINITY) ? __fsub_rn(t, a) : -INFINITY;
@@ -130,40 +163,51 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
   bool ok = true;
   if (nv > 0 && !mbar_wait_sleep(&bar, 0u)) ok = false;
 
-  // ---- (1) the target row's maximum ---------------------------------------
-  float mx = -INFINITY;
-  bool bad = false;
-  for (int v = tid; v < nv; v += kThreadsS) {
-    float xt[VEC], xa[VEC];
-    Staged<E>::unpack(tsl[v], xt);
-    Staged<E>::unpack(asl[v], xa);
-#pragma unroll
-    for (int k = 0; k < VEC; ++k) {
-      mx = fmaxf(mx, xt[k]);
-      bad |= (!(xt[k] <= FLT_MAX) && !(xt[k] == -INFINITY)) ||
-             (!(xa[k] <= FLT_MAX) && !(xa[k] == -INFINITY));
+  // ---- (1) the target row's maximum and the amateur's normaliser ---------
+  // Maxima propagate NaN, so a NaN or +inf in either row shows in them.
+  float mt = -INFINITY, ma = -INFINITY;
+  RowAcc Aa{-INFINITY, 0.f};
+  for (int v = tid; v < nv; v += 2 * kThreadsS) {
+    uint4 wa[2];
+    const int n2 = v + kThreadsS < nv ? 2 : 1;
+    mt = nan_max(mt, vec_max_nan<E>(tsl[v]));
+    wa[0] = asl[v];
+    ma = nan_max(ma, vec_max_nan<E>(wa[0]));
+    if (n2 > 1) {
+      mt = nan_max(mt, vec_max_nan<E>(tsl[v + kThreadsS]));
+      wa[1] = asl[v + kThreadsS];
+      ma = nan_max(ma, vec_max_nan<E>(wa[1]));
     }
+    if (has_draft) acc_vectors<E>(Aa, wa, n2, s);
   }
+  const bool bad = isnan(mt) || mt == INFINITY || isnan(ma) || ma == INFINITY;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) s_wmax[warp] = mx;
+  for (int o = 16; o > 0; o >>= 1) mt = nan_max(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+  warp_merge_scaled(Aa.ms, Aa.z);
+  if (lane == 0) {
+    s_wmax[warp] = mt;
+    s_warp[warp] = Norm4{-INFINITY, 0.f, Aa.ms, Aa.z};
+  }
   if (__syncthreads_or(bad) && tid == 0) s_bad = 1;
   cluster_wait();  // every CTA of the cluster has started
   if (warp == 0) {
     float m = lane < kWarpsS ? s_wmax[lane] : -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int o = 16; o > 0; o >>= 1) m = nan_max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane < C) *cluster.map_shared_rank(&s_pmax[rank], lane) = m;
   }
   cluster.sync();
   float M = -INFINITY;
-  for (int r = 0; r < C; ++r) M = fmaxf(M, s_pmax[r]);
+  for (int r = 0; r < C; ++r) M = nan_max(M, s_pmax[r]);
   const float thr = __double2float_ru(__dadd_rn(static_cast<double>(M), L));
 
-  // ---- (2) normalisers of the contrast on the head and of the amateur -----
-  RowAcc Ac{-INFINITY, 0.f}, Aa{-INFINITY, 0.f};
+  // ---- (2) the contrast's normaliser on the head --------------------------
+  // The head holds the tokens within T ln(1/alpha) of the maximum: a vector
+  // with none of them adds nothing and is skipped after one packed maximum.
+  RowAcc Ac{-INFINITY, 0.f};
   bool unbounded = false;  // a head token the amateur gives no mass
   for (int v = tid; v < nv; v += kThreadsS) {
+    if (!(vec_max<E>(tsl[v]) >= thr)) continue;
     float xt[VEC], xa[VEC], xc[VEC];
     Staged<E>::unpack(tsl[v], xt);
     Staged<E>::unpack(asl[v], xa);
@@ -173,11 +217,12 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
       unbounded |= xc[k] == INFINITY;
     }
     acc_floats<VEC>(Ac, xc, s);
-    if (has_draft) acc_floats<VEC>(Aa, xa, s);
   }
   warp_merge_scaled(Ac.ms, Ac.z);
-  warp_merge_scaled(Aa.ms, Aa.z);
-  if (lane == 0) s_warp[warp] = Norm4{Ac.ms, Ac.z, Aa.ms, Aa.z};
+  if (lane == 0) {
+    s_warp[warp].msc = Ac.ms;
+    s_warp[warp].zc = Ac.z;
+  }
   if (__syncthreads_or(unbounded) && tid == 0) s_bad = 1;
   if (warp == 0) {
     Norm4 m = lane < kWarpsS ? s_warp[lane] : Norm4{-INFINITY, 0.f, -INFINITY, 0.f};
@@ -249,19 +294,16 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
   for (int rnd = 0; rnd < 2; ++rnd) {
     for (int k = 0; k < ntl; ++k) {
       const int v = k * kThreadsS + tid;
-      float xc[VEC], xa[VEC], r[VEC];
-      if (v < nv) {
-        float xt[VEC];
+      unsigned long long w = 0;  // P_n is 0 off the head, and so is max(0, P_n - q)
+      if (v < nv && vec_max<E>(tsl[v]) >= thr) {
+        float xt[VEC], xa[VEC], xc[VEC], r[VEC];
         Staged<E>::unpack(tsl[v], xt);
         Staged<E>::unpack(asl[v], xa);
 #pragma unroll
         for (int q = 0; q < VEC; ++q) xc[q] = contrast(xt[q], xa[q], thr);
-      } else {
-#pragma unroll
-        for (int q = 0; q < VEC; ++q) xc[q] = xa[q] = -INFINITY;
+        w = vec_weight_scaled<VEC>(xc, xa, MSc, invZc, MSa, invZa, s, residual, r);
       }
-      const unsigned long long w = warp_sum_mass(
-          vec_weight_scaled<VEC>(xc, xa, MSc, invZc, MSa, invZa, s, residual, r));
+      w = warp_sum_mass(w);
       if (lane == 0) tws[k * kWarpsS + warp] = w;
     }
     __syncthreads();
