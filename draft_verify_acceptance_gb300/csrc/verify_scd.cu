@@ -52,6 +52,7 @@ constexpr int kMaxCS = 8;
 constexpr long long kPairBytes2 = 96 * 1024;   // both slices, two CTAs per SM
 constexpr long long kPairBytes1 = 200 * 1024;  // both slices, one CTA per SM
 constexpr int kCopyVecS = 2048;                // vectors per bulk copy (32 KiB)
+constexpr int kChunksS = 4;                    // staging chunks (barriers) per slice
 
 struct __align__(16) Norm4 {
   float msc, zc, msa, za;
@@ -134,7 +135,8 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
   uint4* tsl = smem;                        // [nvs] target slice
   uint4* asl = smem + nvs;                  // [nvs] amateur slice
   unsigned long long* tws = reinterpret_cast<unsigned long long*>(smem + 2 * nvs);
-  __shared__ __align__(8) unsigned long long bar;
+  __shared__ __align__(8) unsigned long long bar[kChunksS];
+  __shared__ float s_x[2];                  // t[x_i], a[x_i], pushed by the CTA holding x_i
   __shared__ float s_wmax[kWarpsS];
   __shared__ float s_pmax[kMaxCS];          // pushed by each rank
   __shared__ Norm4 s_warp[kWarpsS];
@@ -145,31 +147,46 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
   const size_t roff = static_cast<size_t>(row) * nvec;
   const uint4* tsrc = static_cast<const uint4*>(a.target) + roff + v0;
   const uint4* asrc = static_cast<const uint4*>(amateur) + roff + v0;
+  // the slice arrives in kChunksS chunks, each on its own barrier, so the
+  // first pass starts on the first chunk while the others are in flight
+  const int chunk = (nv + kChunksS - 1) / kChunksS;
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    for (int c = 0; c < kChunksS; ++c) mbar_init(&bar[c], 1);
     fence_barrier_init();
     s_bad = 0;
   }
   __syncthreads();
-  if (tid == 0 && nv > 0) {
-    mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nv) * 32u);
-    for (int c0 = 0; c0 < nv; c0 += kCopyVecS) {
-      const uint32_t len = static_cast<uint32_t>(min(kCopyVecS, nv - c0)) * 16u;
-      bulk_load(tsl + c0, tsrc + c0, len, &bar);
-      bulk_load(asl + c0, asrc + c0, len, &bar);
+  if (tid == 0) {
+    for (int c = 0; c < kChunksS; ++c) {
+      const int lo = min(c * chunk, nv), hi = min(lo + chunk, nv);
+      if (hi <= lo) continue;
+      mbar_arrive_expect_tx(&bar[c], static_cast<uint32_t>(hi - lo) * 32u);
+      for (int c0 = lo; c0 < hi; c0 += kCopyVecS) {
+        const uint32_t len = static_cast<uint32_t>(min(kCopyVecS, hi - c0)) * 16u;
+        bulk_load(tsl + c0, tsrc + c0, len, &bar[c]);
+        bulk_load(asl + c0, asrc + c0, len, &bar[c]);
+      }
     }
   }
   cluster_arrive_relaxed();  // matched before the first DSMEM push
+  // the draft token of this row and whether this CTA's slice holds it
+  int xr = 0;
+  if (has_draft) xr = a.tokens[static_cast<size_t>(b) * K + i];
+  const int xcl = min(max(xr, 0), a.V - 1);
+  const bool holds_x = has_draft && xcl / VEC >= v0 && xcl / VEC < v0 + nv;
   bool ok = true;
-  if (nv > 0 && !mbar_wait_sleep(&bar, 0u)) ok = false;
 
   // ---- (1) the target row's maximum and the amateur's normaliser ---------
   // Maxima propagate NaN, so a NaN or +inf in either row shows in them.
   float mt = -INFINITY, ma = -INFINITY;
   RowAcc Aa{-INFINITY, 0.f};
-  for (int v = tid; v < nv; v += 2 * kThreadsS) {
+  for (int c = 0; c < kChunksS; ++c) {
+   const int lo = min(c * chunk, nv), hi = min(lo + chunk, nv);
+   if (hi <= lo) continue;
+   if (!mbar_wait_sleep(&bar[c], 0u)) ok = false;
+   for (int v = lo + tid; v < hi; v += 2 * kThreadsS) {
     uint4 wa[2];
-    const int n2 = v + kThreadsS < nv ? 2 : 1;
+    const int n2 = v + kThreadsS < hi ? 2 : 1;
     mt = nan_max(mt, vec_max_nan<E>(tsl[v]));
     wa[0] = asl[v];
     ma = nan_max(ma, vec_max_nan<E>(wa[0]));
@@ -179,6 +196,7 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
       ma = nan_max(ma, vec_max_nan<E>(wa[1]));
     }
     if (has_draft) acc_vectors<E>(Aa, wa, n2, s);
+   }
   }
   const bool bad = isnan(mt) || mt == INFINITY || isnan(ma) || ma == INFINITY;
 #pragma unroll
@@ -223,6 +241,15 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
     s_warp[warp].msc = Ac.ms;
     s_warp[warp].zc = Ac.z;
   }
+  if (holds_x && tid == 0) {
+    const int j = xcl - static_cast<int>(v0) * VEC;
+    const float tx = staged_elem<E>(tsl, j), ax = staged_elem<E>(asl, j);
+    for (int r = 0; r < C; ++r) {
+      float* dst = cluster.map_shared_rank(s_x, r);
+      dst[0] = tx;
+      dst[1] = ax;
+    }
+  }
   if (__syncthreads_or(unbounded) && tid == 0) s_bad = 1;
   if (warp == 0) {
     Norm4 m = lane < kWarpsS ? s_warp[lane] : Norm4{-INFINITY, 0.f, -INFINITY, 0.f};
@@ -243,25 +270,22 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
   const float uK = a.uniforms[static_cast<size_t>(b) * K1 + K];
 
   // ---- accept test and whether this row needs a draw (rank 0) -------------
+  // A row draws when its draft token is rejected and no earlier position has
+  // been rejected yet, and the bonus row always; the sequence's last arrival
+  // picks the first rejected row's candidate.
   if (rank == 0 && tid == 0) {
     SeqState* st = a.seq + b;
-    int err = 0;
-    if (!norm_ok) err |= kDataNonfiniteLogit;
+    int err = norm_ok ? 0 : kDataNonfiniteLogit;
     bool need = true;
     if (has_draft) {
-      const int xr = a.tokens[static_cast<size_t>(b) * K + i];
-      const int x = min(max(xr, 0), a.V - 1);
       const float ui = a.uniforms[static_cast<size_t>(b) * K1 + i];
-      const void* trow = static_cast<const char*>(a.target) + roff * 16;
-      const void* arow = static_cast<const char*>(amateur) + roff * 16;
-      const float tx = load_one<E>(trow, x), ax = load_one<E>(arow, x);
-      const float cx = contrast(tx, ax, thr);
+      const float cx = contrast(s_x[0], s_x[1], thr);
       const float px = __fmul_rn(ex2(__fmaf_rn(cx, s, -MSc)), invZc);
-      const float qx = __fmul_rn(ex2(__fmaf_rn(ax, s, -MSa)), invZa);
+      const float qx = __fmul_rn(ex2(__fmaf_rn(s_x[1], s, -MSa)), invZa);
       const bool accept = ui * qx < px;
       if (a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
       if (a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
-      if (xr != x) err |= kDataTokenRange;
+      if (xr != xcl) err |= kDataTokenRange;
       if (!(ui >= 0.f && ui < 1.f)) err |= kDataUniformRange;
       if (qx > 0.f && fabsf(ui - fminf(1.f, px / qx)) < kBandF)
         atomicOr(&st->near_mask, 1ull << i);
