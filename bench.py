@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table and the CPU baseline")
+    ap.add_argument("--line", default=None,
+                    help="time one contrastive-verify or rejection-cut workload alone "
+                         "(--steps launches) and print its line")
     return ap.parse_args()
 
 
@@ -168,6 +171,7 @@ KERNEL_SOURCES = {
                            "launch.h"],
     "sample_kernel": ["verify_sample.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
     "cut_warp_kernel": ["rejection_cut.cu", "launch.h"],
+    "scd_row_kernel": ["verify_scd.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
 }
 
 
@@ -388,13 +392,13 @@ def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
             table[name + "+early_exit"] = early_exit_line(binding, inp, steps, dev, l2, peak, sec)
             table[name + "+draft_sample"] = draft_sample_line(binding, inp, steps, dev, l2, peak)
     for name, spec in W.SCD_WORKLOADS.items():
-        table[name] = scd_line(binding, spec, steps, dev, l2, peak)
+        table[name] = scd_line(binding, name, spec, steps, dev, l2, peak)
     for name, spec in W.REJECTION_WORKLOADS.items():
-        table[name] = rejection_cut_line(binding, spec, steps, dev, l2, peak)
+        table[name] = rejection_cut_line(binding, name, spec, steps, dev, l2, peak)
     return table
 
 
-def scd_line(binding, spec, steps, dev, l2, peak):
+def scd_line(binding, name, spec, steps, dev, l2, peak):
     """Speculative contrastive decoding's verify step (bytes: every expert
     and amateur row read once, the tokens, the uniforms and the outputs),
     graph-replayed over rotating input copies > 2x L2 like the rest."""
@@ -402,7 +406,7 @@ def scd_line(binding, spec, steps, dev, l2, peak):
     from draft_verify_acceptance_gb300 import workloads as W
     spec = dict(spec)
     alpha = spec.pop("alpha")
-    inp = W.make_scd_inputs(seed=0, **spec)
+    inp = W.make_scd_inputs(seed=0, name=name, **spec)
     B, K, V = inp.B, inp.K, inp.V
     es = inp.target.element_size()
     nbytes = 2 * B * (K + 1) * V * es + B * K * 4 + B * (K + 1) * 4 + B * 4 + B * (K + 1) * 4
@@ -443,10 +447,11 @@ def scd_line(binding, spec, steps, dev, l2, peak):
     torch.cuda.empty_cache()
     return {"us_per_step": sec * 1e6, "positions_per_s": B * K / sec, "bytes": nbytes,
             "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
-            "kernel": "scd_row_kernel", "mean_accepted_len": mean_n}
+            "kernel": "scd_row_kernel", "mean_accepted_len": mean_n,
+            "traffic": committed_traffic(inp.name, "scd_row_kernel")}
 
 
-def rejection_cut_line(binding, spec, steps, dev, l2, peak):
+def rejection_cut_line(binding, name, spec, steps, dev, l2, peak):
     """Speculative Rejection's cut over G prompts of N scores (bytes: the
     scores read, the kept-index rows, r_cut and the counts written),
     graph-replayed over rotating score copies > 2x L2; the oracle's time on
@@ -488,6 +493,7 @@ def rejection_cut_line(binding, spec, steps, dev, l2, peak):
     return {"us_per_step": sec * 1e6, "scores_per_s": G * N / sec, "bytes": nbytes,
             "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
             "kernel": "cut_warp_kernel" if N <= 1024 else "cut_block_kernel",
+            "traffic": committed_traffic(name, "cut_warp_kernel") if N <= 1024 else None,
             "cpu_baseline": {"value": G * N / cpu_sec, "unit": "scores/s",
                              "cores": oracle.max_threads(), "kind": "oracle",
                              "sample": f"the whole batch ({G} x {N}), once"}}
@@ -636,8 +642,29 @@ def run_reference(args, rank, world):
     }))
 
 
+def run_line(args):
+    """One line of the per-workload table on its own (for profiling runs)."""
+    import torch
+    from draft_verify_acceptance_gb300 import binding, workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20)
+    peak, _ = hbm_peak()
+    if args.line in W.SCD_WORKLOADS:
+        res = scd_line(binding, args.line, W.SCD_WORKLOADS[args.line], args.steps, dev, l2, peak)
+    elif args.line in W.REJECTION_WORKLOADS:
+        res = rejection_cut_line(binding, args.line, W.REJECTION_WORKLOADS[args.line], args.steps,
+                                 dev, l2, peak)
+    else:
+        raise SystemExit(f"unknown line {args.line!r}")
+    print(json.dumps({"line": args.line, **res}))
+
+
 def main():
     args = parse()
+    if args.line:
+        run_line(args)
+        return
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

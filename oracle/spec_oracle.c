@@ -45,7 +45,8 @@
  *   - greedy: argmax of the raw logit values (bf16 widens exactly), lowest
  *     index on ties.
  *   - contrastive target ([SCD] "Speculative Contrastive Decoding"; the
- *     formula was lost from the page, so parity of P_n itself is unpinned):
+ *     formula was lost from the page: contrastive_row is "parity unpinned",
+ *     only its two limits and the verify step around it are pinned):
  *     contrastive decoding's log p_e - log p_a over the plausible head
  *     { p_e >= alpha * max p_e }, normalised there (contrastive_row); the
  *     amateur supplies the draft distribution q and its row K enters only
