@@ -16,20 +16,27 @@
 // test is taken exactly: thr = the double M + T ln alpha rounded up to fp32,
 // and t_j >= thr in fp32 (thr is the smallest float >= M + T ln alpha).
 //
-// Design: one cluster of C CTAs per row (b, i), i = 0..K.  Each CTA copies
-// its slice of the target row and of the amateur row into shared memory once
-// (bulk copies), so both rows cross HBM once.  From shared memory: (1) the
-// target row's maximum, exchanged over the cluster (DSMEM), which fixes the
-// head; (2) the online normalisers of the contrast (t - a) * s on the head
-// and, at draft positions, of the amateur a * s, merged in rank order; rank
-// 0 then runs the accept test of x_i and decides whether the row needs a
-// draw (a rejected draft position with no earlier rejection, or the bonus
-// row); (3) the fixed-point masses of max(0, P_n - q) (or of P_n) per vector,
-// summed per (tile, warp) and per slice, exchanged over the cluster; (4) the
-// CTA holding the draw's threshold finds the token and stores it as the
-// row's candidate.  The rows of a sequence meet through its arrival counter;
-// the last one writes the outputs (the same protocol as the streaming
-// sampler).  Every wait is bounded.
+// Design: one cluster of C CTAs per row (b, i), i = 0..K, each CTA a slice
+// of at most 2048 16-byte vectors of both rows.  (1) One streaming pass
+// reads the slice of the expert row and of the amateur row once from HBM:
+// the expert row's maximum (packed NaN-propagating maxima, which also catch
+// NaN / +inf), the amateur's online normaliser, and the few vectors that may
+// hold head tokens -- a vector is remembered when its maximum is within
+// T ln(1/alpha) of the thread's running maximum, a superset of the final
+// head since the row maximum is at least the running one.  The cluster
+// exchanges maxima and normalisers through DSMEM, which fixes the head.
+// (2) Only remembered vectors at or above the head threshold are read again
+// (from L2) for the contrast's normaliser, merged in rank order; rank 0 runs
+// the accept test of x_i and decides whether the row draws (a rejected draft
+// position with no earlier rejection, or the bonus row).  (3) The fixed-
+// point masses of max(0, P_n - q) (or of P_n) are non-zero only on head
+// vectors, summed per (tile, warp) and per slice, exchanged over the
+// cluster; (4) the CTA holding the draw's threshold finds the token and
+// stores it as the row's candidate.  The rows of a sequence meet through its
+// arrival counter; the last one writes the outputs (the same protocol as the
+// streaming sampler).  A thread that meets more candidate vectors than it
+// can remember (alpha near 0, where the head is most of the row) makes its
+// CTA read its slice again in (2) and (3) instead.
 #include <cooperative_groups.h>
 
 #include <cfloat>
@@ -49,10 +56,10 @@ namespace {
 constexpr int kThreadsS = 256;
 constexpr int kWarpsS = kThreadsS / 32;
 constexpr int kMaxCS = 8;
-constexpr long long kPairBytes2 = 96 * 1024;   // both slices, two CTAs per SM
-constexpr long long kPairBytes1 = 200 * 1024;  // both slices, one CTA per SM
-constexpr int kCopyVecS = 2048;                // vectors per bulk copy (32 KiB)
-constexpr int kChunksS = 4;                    // staging chunks (barriers) per slice
+constexpr int kSliceVecS = 2048;  // vectors of each row per CTA (8 tiles) when the cluster allows
+constexpr int kMaxTilesS = 64;    // tiles of kThreadsS vectors per slice at most
+constexpr int kCand = 8;          // head-candidate vectors remembered per thread
+constexpr int kU = 4;             // vectors of each row in flight per thread
 
 struct __align__(16) Norm4 {
   float msc, zc, msa, za;
@@ -114,8 +121,8 @@ __device__ __forceinline__ float contrast(float t, float a, float thr) {
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kThreadsS, 2)
-scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, double L) {
+__global__ void __launch_bounds__(kThreadsS, 4)
+scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, double L, float Lmag) {
   constexpr int VEC = Staged<E>::kVec;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
@@ -129,74 +136,84 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
   const long long v0 = (nvec * rank) >> lgC;
   const int nv = static_cast<int>(((nvec * (rank + 1)) >> lgC) - v0);
   const int ntl = (nv + kThreadsS - 1) / kThreadsS;
-  const long long nvs = (nvec + C - 1) >> lgC;
 
-  extern __shared__ __align__(128) uint4 smem[];
-  uint4* tsl = smem;                        // [nvs] target slice
-  uint4* asl = smem + nvs;                  // [nvs] amateur slice
-  unsigned long long* tws = reinterpret_cast<unsigned long long*>(smem + 2 * nvs);
-  __shared__ __align__(8) unsigned long long bar[kChunksS];
-  __shared__ float s_x[2];                  // t[x_i], a[x_i], pushed by the CTA holding x_i
+  extern __shared__ unsigned long long tws[];  // [ntl][warps] masses
+  __shared__ uint16_t s_ck[kCand][kThreadsS];  // head-candidate tiles of each thread
+  __shared__ float s_cm[kCand][kThreadsS];     // and their vectors' maxima
   __shared__ float s_wmax[kWarpsS];
-  __shared__ float s_pmax[kMaxCS];          // pushed by each rank
   __shared__ Norm4 s_warp[kWarpsS];
-  __shared__ Norm4 s_part[kMaxCS];          // pushed by each rank
+  __shared__ Norm4 s_part1[kMaxCS];            // (row max, amateur normaliser), pushed by each rank
+  __shared__ Norm4 s_part[kMaxCS];             // contrast normaliser, pushed by each rank
   __shared__ unsigned long long s_mass[kMaxCS];
-  __shared__ int s_need, s_bad;
+  __shared__ int s_need, s_bad, s_rescan;
 
   const size_t roff = static_cast<size_t>(row) * nvec;
-  const uint4* tsrc = static_cast<const uint4*>(a.target) + roff + v0;
-  const uint4* asrc = static_cast<const uint4*>(amateur) + roff + v0;
-  // the slice arrives in kChunksS chunks, each on its own barrier, so the
-  // first pass starts on the first chunk while the others are in flight
-  const int chunk = (nv + kChunksS - 1) / kChunksS;
+  const uint4* trow = static_cast<const uint4*>(a.target) + roff + v0;
+  const uint4* arow = static_cast<const uint4*>(amateur) + roff + v0;
   if (tid == 0) {
-    for (int c = 0; c < kChunksS; ++c) mbar_init(&bar[c], 1);
-    fence_barrier_init();
     s_bad = 0;
+    s_rescan = 0;
+  }
+  // the draft token and its two logits, read early by the thread that takes
+  // the accept test
+  int xr = 0, xcl = 0;
+  float tx = 0.f, ax = 0.f;
+  if (has_draft && rank == 0 && tid == 0) {
+    xr = a.tokens[static_cast<size_t>(b) * K + i];
+    xcl = min(max(xr, 0), a.V - 1);
+    tx = load_one<E>(static_cast<const uint4*>(a.target) + roff, xcl);
+    ax = load_one<E>(static_cast<const uint4*>(amateur) + roff, xcl);
   }
   __syncthreads();
-  if (tid == 0) {
-    for (int c = 0; c < kChunksS; ++c) {
-      const int lo = min(c * chunk, nv), hi = min(lo + chunk, nv);
-      if (hi <= lo) continue;
-      mbar_arrive_expect_tx(&bar[c], static_cast<uint32_t>(hi - lo) * 32u);
-      for (int c0 = lo; c0 < hi; c0 += kCopyVecS) {
-        const uint32_t len = static_cast<uint32_t>(min(kCopyVecS, hi - c0)) * 16u;
-        bulk_load(tsl + c0, tsrc + c0, len, &bar[c]);
-        bulk_load(asl + c0, asrc + c0, len, &bar[c]);
-      }
-    }
-  }
   cluster_arrive_relaxed();  // matched before the first DSMEM push
-  // the draft token of this row and whether this CTA's slice holds it
-  int xr = 0;
-  if (has_draft) xr = a.tokens[static_cast<size_t>(b) * K + i];
-  const int xcl = min(max(xr, 0), a.V - 1);
-  const bool holds_x = has_draft && xcl / VEC >= v0 && xcl / VEC < v0 + nv;
-  bool ok = true;
 
-  // ---- (1) the target row's maximum and the amateur's normaliser ---------
-  // Maxima propagate NaN, so a NaN or +inf in either row shows in them.
+  // ---- (1) one streaming pass over both rows ------------------------------
+  // The expert row's maximum and NaN checks (packed NaN-propagating maxima),
+  // the amateur's online normaliser, and the vectors that may hold head
+  // tokens: a vector is remembered when its maximum is within T ln(1/alpha)
+  // of this thread's running maximum (rounded down: every vector of the
+  // final head is remembered, since the row maximum is at least the running
+  // one).  A thread with more than kCand of them makes its CTA rescan.
   float mt = -INFINITY, ma = -INFINITY;
   RowAcc Aa{-INFINITY, 0.f};
-  for (int c = 0; c < kChunksS; ++c) {
-   const int lo = min(c * chunk, nv), hi = min(lo + chunk, nv);
-   if (hi <= lo) continue;
-   if (!mbar_wait_sleep(&bar[c], 0u)) ok = false;
-   for (int v = lo + tid; v < hi; v += 2 * kThreadsS) {
-    uint4 wa[2];
-    const int n2 = v + kThreadsS < hi ? 2 : 1;
-    mt = nan_max(mt, vec_max_nan<E>(tsl[v]));
-    wa[0] = asl[v];
-    ma = nan_max(ma, vec_max_nan<E>(wa[0]));
-    if (n2 > 1) {
-      mt = nan_max(mt, vec_max_nan<E>(tsl[v + kThreadsS]));
-      wa[1] = asl[v + kThreadsS];
-      ma = nan_max(ma, vec_max_nan<E>(wa[1]));
+  int nc = 0;
+  for (int k0 = 0; k0 < ntl; k0 += kU) {
+    uint4 wt[kU], wa[kU];
+    int nval = 0;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = (k0 + u) * kThreadsS + tid;
+      if (k0 + u < ntl && v < nv) {
+        wt[u] = ld_stream_v4(trow + v);
+        wa[u] = ld_stream_v4(arow + v);
+        nval = u + 1;
+      }
     }
-    if (has_draft) acc_vectors<E>(Aa, wa, n2, s);
-   }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (u < nval) {
+        const float vm = vec_max_nan<E>(wt[u]);
+        mt = nan_max(mt, vm);
+        ma = nan_max(ma, vec_max_nan<E>(wa[u]));
+        if (vm >= __fsub_rd(mt, Lmag)) {
+          if (nc < kCand) {
+            s_ck[nc][tid] = static_cast<uint16_t>(k0 + u);
+            s_cm[nc][tid] = vm;
+          }
+          ++nc;
+        }
+      }
+    }
+    if (has_draft) {
+#pragma unroll
+      for (int u = 0; u < kU; u += 2) {
+        const int n2 = min(max(nval - u, 0), 2);
+        if (n2 > 0) {
+          const uint4 w2[2] = {wa[u], wa[u + 1]};
+          acc_vectors<E>(Aa, w2, n2, s);
+        }
+      }
+    }
   }
   const bool bad = isnan(mt) || mt == INFINITY || isnan(ma) || ma == INFINITY;
 #pragma unroll
@@ -207,28 +224,46 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
     s_warp[warp] = Norm4{-INFINITY, 0.f, Aa.ms, Aa.z};
   }
   if (__syncthreads_or(bad) && tid == 0) s_bad = 1;
+  if (__syncthreads_or(nc > kCand) && tid == 0) s_rescan = 1;
   cluster_wait();  // every CTA of the cluster has started
   if (warp == 0) {
     float m = lane < kWarpsS ? s_wmax[lane] : -INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = nan_max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane < C) *cluster.map_shared_rank(&s_pmax[rank], lane) = m;
+    Norm4 p = lane < kWarpsS ? s_warp[lane] : Norm4{-INFINITY, 0.f, -INFINITY, 0.f};
+    warp_merge_scaled(p.msa, p.za);
+    p.msc = m;  // the slice's maximum rides in the first field
+    if (lane < C) *cluster.map_shared_rank(&s_part1[rank], lane) = p;
   }
   cluster.sync();
-  float M = -INFINITY;
-  for (int r = 0; r < C; ++r) M = nan_max(M, s_pmax[r]);
+  float M = -INFINITY, MSa = -INFINITY, Za = 0.f;
+  for (int r = 0; r < C; ++r) {  // rank order: the same bits in every CTA
+    M = nan_max(M, s_part1[r].msc);
+    merge_scaled(MSa, Za, s_part1[r].msa, s_part1[r].za);
+  }
   const float thr = __double2float_ru(__dadd_rn(static_cast<double>(M), L));
+  const bool rescan = s_rescan != 0;
+  const int ncs = min(nc, kCand);
 
   // ---- (2) the contrast's normaliser on the head --------------------------
-  // The head holds the tokens within T ln(1/alpha) of the maximum: a vector
-  // with none of them adds nothing and is skipped after one packed maximum.
+  // Only remembered vectors at or above the threshold are read again (from
+  // L2, shortly after the stream); a rescanning CTA reads its slice again.
   RowAcc Ac{-INFINITY, 0.f};
   bool unbounded = false;  // a head token the amateur gives no mass
-  for (int v = tid; v < nv; v += kThreadsS) {
-    if (!(vec_max<E>(tsl[v]) >= thr)) continue;
+  for (int c = 0; c < (rescan ? ntl : ncs); ++c) {
+    int v;
+    if (rescan) {
+      v = c * kThreadsS + tid;
+      if (v >= nv) break;
+    } else {
+      if (!(s_cm[c][tid] >= thr)) continue;
+      v = s_ck[c][tid] * kThreadsS + tid;
+    }
+    const uint4 wt = __ldg(trow + v);
+    if (!(vec_max<E>(wt) >= thr)) continue;
     float xt[VEC], xa[VEC], xc[VEC];
-    Staged<E>::unpack(tsl[v], xt);
-    Staged<E>::unpack(asl[v], xa);
+    Staged<E>::unpack(wt, xt);
+    Staged<E>::unpack(__ldg(arow + v), xa);
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
       xc[k] = contrast(xt[k], xa[k], thr);
@@ -241,28 +276,15 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
     s_warp[warp].msc = Ac.ms;
     s_warp[warp].zc = Ac.z;
   }
-  if (holds_x && tid == 0) {
-    const int j = xcl - static_cast<int>(v0) * VEC;
-    const float tx = staged_elem<E>(tsl, j), ax = staged_elem<E>(asl, j);
-    for (int r = 0; r < C; ++r) {
-      float* dst = cluster.map_shared_rank(s_x, r);
-      dst[0] = tx;
-      dst[1] = ax;
-    }
-  }
   if (__syncthreads_or(unbounded) && tid == 0) s_bad = 1;
   if (warp == 0) {
     Norm4 m = lane < kWarpsS ? s_warp[lane] : Norm4{-INFINITY, 0.f, -INFINITY, 0.f};
     warp_merge_scaled(m.msc, m.zc);
-    warp_merge_scaled(m.msa, m.za);
     if (lane < C) *cluster.map_shared_rank(&s_part[rank], lane) = m;
   }
   cluster.sync();
-  float MSc = -INFINITY, Zc = 0.f, MSa = -INFINITY, Za = 0.f;
-  for (int r = 0; r < C; ++r) {  // rank order: the same bits in every CTA
-    merge_scaled(MSc, Zc, s_part[r].msc, s_part[r].zc);
-    merge_scaled(MSa, Za, s_part[r].msa, s_part[r].za);
-  }
+  float MSc = -INFINITY, Zc = 0.f;
+  for (int r = 0; r < C; ++r) merge_scaled(MSc, Zc, s_part[r].msc, s_part[r].zc);
   const bool norm_ok = isfinite(MSc) && isfinite(Zc) && Zc > 0.f &&
                        (!has_draft || (isfinite(MSa) && isfinite(Za) && Za > 0.f));
   const float invZc = norm_ok ? 1.f / Zc : 0.f;
@@ -279,9 +301,9 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
     bool need = true;
     if (has_draft) {
       const float ui = a.uniforms[static_cast<size_t>(b) * K1 + i];
-      const float cx = contrast(s_x[0], s_x[1], thr);
+      const float cx = contrast(tx, ax, thr);
       const float px = __fmul_rn(ex2(__fmaf_rn(cx, s, -MSc)), invZc);
-      const float qx = __fmul_rn(ex2(__fmaf_rn(s_x[1], s, -MSa)), invZa);
+      const float qx = __fmul_rn(ex2(__fmaf_rn(ax, s, -MSa)), invZa);
       const bool accept = ui * qx < px;
       if (a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
       if (a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
@@ -303,9 +325,8 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
     }
     for (int r = 0; r < C; ++r) *cluster.map_shared_rank(&s_need, r) = need ? 1 : 0;
   }
-  // any CTA that saw a bad element or a lost copy reports it
-  if (tid == 0 && (s_bad || !ok) && a.status)
-    atomicOr(a.status, (s_bad ? kDataNonfiniteLogit : 0) | (ok ? 0 : kWaitTimeout));
+  // any CTA that saw a bad element reports it
+  if (tid == 0 && s_bad && a.status) atomicOr(a.status, kDataNonfiniteLogit);
   cluster.sync();
   if (!s_need) {
     if (rank == 0 && warp == 0) warp_arrive_and_finalize(a, b);
@@ -313,19 +334,32 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
   }
 
   // ---- (3) fixed-point masses of max(0, P_n - q) (or P_n) -----------------
+  // P_n is 0 off the head, and so is max(0, P_n - q): only head vectors have
+  // mass; the per-(tile, warp) sums keep the slice's order for the crossing.
   bool residual = has_draft;
   unsigned long long S = 0;
   for (int rnd = 0; rnd < 2; ++rnd) {
+    int ci = 0;
     for (int k = 0; k < ntl; ++k) {
       const int v = k * kThreadsS + tid;
-      unsigned long long w = 0;  // P_n is 0 off the head, and so is max(0, P_n - q)
-      if (v < nv && vec_max<E>(tsl[v]) >= thr) {
-        float xt[VEC], xa[VEC], xc[VEC], r[VEC];
-        Staged<E>::unpack(tsl[v], xt);
-        Staged<E>::unpack(asl[v], xa);
+      bool look = false;
+      if (rescan) {
+        look = v < nv;
+      } else {
+        while (ci < ncs && s_ck[ci][tid] < k) ++ci;
+        look = ci < ncs && s_ck[ci][tid] == k && s_cm[ci][tid] >= thr;
+      }
+      unsigned long long w = 0;
+      if (look) {
+        const uint4 wt = __ldg(trow + v);
+        if (vec_max<E>(wt) >= thr) {
+          float xt[VEC], xa[VEC], xc[VEC], r[VEC];
+          Staged<E>::unpack(wt, xt);
+          Staged<E>::unpack(__ldg(arow + v), xa);
 #pragma unroll
-        for (int q = 0; q < VEC; ++q) xc[q] = contrast(xt[q], xa[q], thr);
-        w = vec_weight_scaled<VEC>(xc, xa, MSc, invZc, MSa, invZa, s, residual, r);
+          for (int q = 0; q < VEC; ++q) xc[q] = contrast(xt[q], xa[q], thr);
+          w = vec_weight_scaled<VEC>(xc, xa, MSc, invZc, MSa, invZa, s, residual, r);
+        }
       }
       w = warp_sum_mass(w);
       if (lane == 0) tws[k * kWarpsS + warp] = w;
@@ -389,8 +423,8 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
     float xc[VEC], xa[VEC], r[VEC];
     if (v < nv) {
       float xt[VEC];
-      Staged<E>::unpack(tsl[v], xt);
-      Staged<E>::unpack(asl[v], xa);
+      Staged<E>::unpack(__ldg(trow + v), xt);
+      Staged<E>::unpack(__ldg(arow + v), xa);
 #pragma unroll
       for (int q = 0; q < VEC; ++q) xc[q] = contrast(xt[q], xa[q], thr);
     } else {
@@ -424,30 +458,22 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
 }  // namespace
 
 // Cluster size for row pairs of nvec vectors: the smallest C in {1, 2, 4, 8}
-// whose two slices fit kPairBytes2 (two CTAs per SM), else 8 if they fit
-// kPairBytes1; 0 when the rows are too long.
+// whose slices hold at most kSliceVecS vectors, else 8 while a slice stays
+// within kMaxTilesS tiles; 0 when the rows are too long.
 int scd_cluster(long long nvec) {
   for (int C = 1; C <= kMaxCS; C *= 2)
-    if (((nvec + C - 1) / C) * 32 <= kPairBytes2) return C;
-  if (((nvec + kMaxCS - 1) / kMaxCS) * 32 <= kPairBytes1) return kMaxCS;
+    if ((nvec + C - 1) / C <= kSliceVecS) return C;
+  if ((nvec + kMaxCS - 1) / kMaxCS <= static_cast<long long>(kMaxTilesS) * kThreadsS) return kMaxCS;
   return 0;
 }
 
 static size_t scd_smem(long long nvec, int C) {
   const long long nvs = (nvec + C - 1) / C;
   const long long ntl = (nvs + kThreadsS - 1) / kThreadsS;
-  return static_cast<size_t>(nvs * 32 + ntl * kWarpsS * 8);
+  return static_cast<size_t>(ntl * kWarpsS * 8);
 }
 
-cudaError_t scd_prepare() {
-  const int smem = static_cast<int>(kPairBytes1) + 8 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(scd_row_kernel<BF16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(scd_row_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-  return e;
-}
+cudaError_t scd_prepare() { return cudaSuccess; }
 
 cudaError_t launch_scd(const VerifyArgs& a, const void* amateur, double L, int C,
                        cudaStream_t stream) {
@@ -455,6 +481,9 @@ cudaError_t launch_scd(const VerifyArgs& a, const void* amateur, double L, int C
   const long long nvec = static_cast<long long>(a.V) * esz / 16;
   const long long grid = static_cast<long long>(a.B) * (a.K + 1) * C;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  // |L| rounded up to fp32, for the candidates' conservative test
+  float Lmag = static_cast<float>(-L);
+  if (static_cast<double>(Lmag) < -L) Lmag = std::nextafter(Lmag, INFINITY);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned int>(grid));
   cfg.blockDim = dim3(kThreadsS);
@@ -467,8 +496,9 @@ cudaError_t launch_scd(const VerifyArgs& a, const void* amateur, double L, int C
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return a.bf16 ? cudaLaunchKernelEx(&cfg, scd_row_kernel<BF16>, a, amateur, nvec, a.scale, L)
-                : cudaLaunchKernelEx(&cfg, scd_row_kernel<F32>, a, amateur, nvec, a.scale, L);
+  return a.bf16
+             ? cudaLaunchKernelEx(&cfg, scd_row_kernel<BF16>, a, amateur, nvec, a.scale, L, Lmag)
+             : cudaLaunchKernelEx(&cfg, scd_row_kernel<F32>, a, amateur, nvec, a.scale, L, Lmag);
 }
 
 }  // namespace specv

@@ -275,9 +275,8 @@ SPEC_API spec_status_t spec_draft_sample(const void* logits, const float* unifor
  *                  1 only the target's argmax (then the result is greedy
  *                  verification's).
  * Rows must be 16-byte aligned (V times the element size a multiple of 16,
- * both bases 16-byte aligned) and a row pair must fit eight CTAs' shared
- * memory (V up to about 400k bf16 / 200k fp32): other calls return
- * SPEC_ERR_UNSUPPORTED.  A NaN or +inf logit in either tensor, or a head
+ * both bases 16-byte aligned): other calls return SPEC_ERR_UNSUPPORTED, as
+ * do rows beyond 2^20 bf16 / 2^19 fp32 logits.  A NaN or +inf logit in either tensor, or a head
  * token whose amateur logit is -inf (an unbounded contrast), sets
  * SPEC_DATA_NONFINITE_LOGIT.  Asynchronous on `stream`.
  */

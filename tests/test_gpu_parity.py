@@ -479,6 +479,11 @@ SCD_CASES = [
     ("scd_f32_alpha0", 8, 3, 5000, torch.float32, 1.0, 0.0, dict(target_std=3.0, amateur_noise=1.0)),
     ("scd_f32_K0", 6, 0, 4096, torch.float32, 1.0, 0.2, dict(target_std=3.0)),
     ("scd_bf16_V1024_T0.05", 16, 3, 1024, torch.bfloat16, 0.05, 0.3, dict(target_std=1.0, amateur_noise=0.1)),
+    # heads too wide to remember vector by vector: the slice is read again
+    ("scd_f32_V152064_alpha0_rescan", 2, 3, 152064, torch.float32, 1.0, 0.0,
+     dict(target_std=3.0, amateur_noise=1.0)),
+    ("scd_f32_V152064_flat_rescan", 2, 3, 152064, torch.float32, 1.0, 0.01,
+     dict(target_std=0.5, amateur_noise=0.3)),
 ]
 
 
