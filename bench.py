@@ -340,7 +340,7 @@ def run_native(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec_max * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded torch CPU generator; recipe in DESIGN.md)",
+        "data": "synthetic (seeded torch CPU generator; recipe in draft_verify_acceptance_gb300/workloads.py)",
         "config": {"workload": args.workload, "B": inp.B, "K": inp.K, "V": inp.V,
                    "logits_dtype": inp.dtype_name,
                    "mode": "greedy" if inp.mode == W.MODE_GREEDY else "sample",

@@ -54,7 +54,7 @@ typedef struct CUstream_st* spec_stream_t;
 typedef enum {
   SPEC_OK = 0,
   SPEC_ERR_INVALID_ARG = 1,  /* bad pointer, size, dtype, mode, temperature or workspace */
-  SPEC_ERR_UNSUPPORTED = 2,  /* valid request beyond this build's limits (K, V, grid) */
+  SPEC_ERR_UNSUPPORTED = 2,  /* valid request beyond the library's limits (K, V, grid) */
   SPEC_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   SPEC_ERR_SCRATCH_LIMIT = 4 /* spec_verify_static: the batch needs more scratch than
                                 SPEC_STATIC_SCRATCH_BYTES */
