@@ -760,6 +760,27 @@ def test_scd_emitted_token_follows_the_contrastive_target():
     assert counts[~head].sum() == 0
     _, pval = stats.chisquare(counts[head], n * pn[head])
     assert pval > 1e-3, pval
+    # once x_0 is accepted, position 1 is a verify step of its own against
+    # P_n at position 1 (accepted x_1 or the residual draw there)
+    head1 = td[1] >= td[1].max() + T * np.log(alpha)
+    pn1 = np.where(head1, np.exp((td[1] - ad[1]) / T), 0.0)
+    pn1 /= pn1.sum()
+    sel = res["accepted_len"] >= 1
+    second = res["out_tokens"][sel, 1]
+    counts1 = np.bincount(second, minlength=V)
+    assert sel.sum() > 10000 and counts1[~head1].sum() == 0
+    _, pval1 = stats.chisquare(counts1[head1], sel.sum() * pn1[head1])
+    assert pval1 > 1e-3, pval1
+    # with both accepted, the bonus token comes from P_n at position K = 2,
+    # built from the expert's and the amateur's rows K
+    head2 = td[2] >= td[2].max() + T * np.log(alpha)
+    pn2 = np.where(head2, np.exp((td[2] - ad[2]) / T), 0.0)
+    pn2 /= pn2.sum()
+    sel2 = res["accepted_len"] == 2
+    counts2 = np.bincount(res["out_tokens"][sel2, 2], minlength=V)
+    assert sel2.sum() > 2000 and counts2[~head2].sum() == 0
+    _, pval2 = stats.chisquare(counts2[head2], sel2.sum() * pn2[head2])
+    assert pval2 > 1e-3, pval2
 
 
 def test_scd_data_errors_and_arguments():
