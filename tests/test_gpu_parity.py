@@ -546,3 +546,47 @@ def test_scd_data_errors_and_workspace(lib):
     assert ok.sum() >= 3
     np.testing.assert_array_equal(g["accepted_len"].cpu().numpy()[ok], ref["accepted_len"][ok])
     assert int(ws.count_nonzero().item()) == 0  # left zero-filled
+
+
+@pytest.mark.parametrize("N", [2, 31, 32, 33, 128, 129, 256, 257, 512, 1023, 1024, 2048, 4097])
+def test_rejection_cut_register_width_edges(lib, N):
+    """Row lengths at and around each register width of the warp kernel
+    (4, 8, 16, 32 scores a lane) and the switch to one CTA per prompt."""
+    s = W.make_scores(5, N, seed=N + 7)
+    for alpha in (0.0, 0.5, 0.999, 1.0):
+        ref = oracle.rejection_cut_ref(s.numpy(), alpha)
+        got = lib.rejection_cut(_dev(s), alpha)
+        torch.cuda.synchronize()
+        _assert_cut_equal(got, ref, f"N={N} alpha={alpha}")
+
+
+def test_rejection_cut_one_prompt_one_score(lib):
+    s = torch.tensor([[-2.5]])
+    r, n, acc = lib.rejection_cut(_dev(s), 0.3)
+    torch.cuda.synchronize()
+    assert r.item() == -2.5 and n.item() == 1 and acc.tolist() == [[0]]
+
+
+SCD_EDGE_CASES = [
+    # name, B, K, V, dtype, T, alpha: the largest K, a tiny vocabulary, one draft position
+    ("scd_f32_Kmax", 3, 64, 256, torch.float32, 1.0, 0.2),
+    ("scd_f32_V4", 64, 2, 4, torch.float32, 1.0, 0.5),
+    ("scd_bf16_V8", 64, 3, 8, torch.bfloat16, 0.8, 0.1),
+    ("scd_bf16_K1", 32, 1, 32000, torch.bfloat16, 1.0, 0.1),
+]
+
+
+@pytest.mark.parametrize("name,B,K,V,dtype,T,alpha", SCD_EDGE_CASES, ids=[c[0] for c in SCD_EDGE_CASES])
+def test_scd_edge_shapes(lib, name, B, K, V, dtype, T, alpha):
+    inp = W.make_scd_inputs(B, K, V, dtype=dtype, temperature=T, name=name, target_std=2.0,
+                            amateur_noise=0.5, seed=zlib.crc32(name.encode()) % 1000)
+    T32 = float(np.float32(T))
+    assert_parity(run_scd(lib, inp, alpha, T32), scd_oracle(inp, alpha, T32), inp, name)
+
+
+def test_scd_empty_batch(lib):
+    t = torch.zeros((0, 3, 1024), device="cuda")
+    n, out = lib.verify_scd(t, t.clone(), torch.zeros((0, 2), dtype=torch.int32, device="cuda"),
+                            torch.zeros((0, 3), device="cuda"), 1.0, 0.1)
+    torch.cuda.synchronize()
+    assert n.numel() == 0 and out.numel() == 0
