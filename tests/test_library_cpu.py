@@ -226,3 +226,19 @@ def test_verify_scd_host_checks(binding):
     wsl = binding.workspace_size(4, 3, 1 << 22, binding.DTYPE_F32, binding.MODE_SAMPLE)
     assert call(V=1 << 22, nbytes=wsl) == binding.ERR_UNSUPPORTED  # a row pair beyond 8 CTAs
     assert call(B=0) == binding.OK
+
+
+def test_c_program_uses_the_boundary_without_python(binding, tmp_path):
+    """A plain C11 program includes the header and links the library (no
+    torch, no Python): it builds with -Wall -Werror and its host-side checks
+    pass without a GPU."""
+    src = os.path.join(os.path.dirname(__file__), "c_abi", "abi_check.c")
+    exe = str(tmp_path / "abi_check")
+    libdir = os.path.dirname(binding.LIB_PATH)
+    cc = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-I",
+                         os.path.dirname(HEADER), src, "-L", libdir, "-lspecverify",
+                         "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    assert "all checks passed" in run.stdout
