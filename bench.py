@@ -175,12 +175,43 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_source_hash(kernel):
-    h = hashlib.sha256()
+def strip_comments(src):
+    """C/C++ source without its comments (string and character literals kept),
+    so that editing a comment leaves a kernel's hash unchanged."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":  # a literal: copy it through, escapes included
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
+def kernel_source_hash(kernel, read=None):
+    """Hash of the sources a kernel is built from, comments and layout left
+    out.  `read(name)` gives a file's text (default: the working tree)."""
     d = os.path.join(ROOT, "draft_verify_acceptance_gb300", "csrc")
+    if read is None:
+        def read(f):
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                return fh.read()
+    h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        code = " ".join(strip_comments(read(f)).split())  # whitespace runs as one space
+        h.update(f.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -82,7 +82,7 @@ cudaError_t launch_row_sample(const void* logits, const float* uniforms, int R, 
                               cudaStream_t stream);
 
 // Speculative contrastive decoding: one cluster of C CTAs per row pair
-// (target, amateur), both staged in shared memory; L = T ln(alpha).
+// (target, amateur), both rows streamed once; L = T ln(alpha).
 int scd_cluster(long long nvec);
 cudaError_t scd_prepare();
 cudaError_t launch_scd(const VerifyArgs& a, const void* amateur, double L, int C,

@@ -112,3 +112,16 @@ def test_hbm_peak_falls_back_without_the_measured_file(monkeypatch, tmp_path):
     assert kind == "fallback" and peak == bench.FALLBACK_HBM_GBS
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000.5}))
     assert bench.hbm_peak() == (7000.5, "measured")
+
+
+def test_kernel_hash_ignores_comments_only():
+    src = 'int f() { return 1; } // note\n/* block\n comment */ const char* s = "// kept";\n'
+    assert bench.strip_comments(src) == 'int f() { return 1; } \n  const char* s = "// kept";\n'
+    files = {f: "" for f in bench.KERNEL_SOURCES["greedy_kernel"]}
+    files["verify_greedy.cu"] = "int x = 1; // one\n"
+    h0 = bench.kernel_source_hash("greedy_kernel", files.get)
+    files["verify_greedy.cu"] = "int x = 1; /* the same code */ // another comment\n"
+    h1 = bench.kernel_source_hash("greedy_kernel", files.get)
+    files["verify_greedy.cu"] = "int x = 2; // one\n"
+    h2 = bench.kernel_source_hash("greedy_kernel", files.get)
+    assert h0 == h1 != h2
