@@ -35,6 +35,7 @@ DEFAULT_WORKLOAD = "greedy_bf16_B64_K8_V32000"
 METRIC = "verified draft positions/sec (B*K/s)"
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
+REF_BUDGET_S = 150.0  # the reference arm's timed CPU work
 
 
 def parse():
@@ -645,17 +646,27 @@ def run_reference(args, rank, world):
         oracle.verify_ref(t[:b], None if d is None else d[:b], x[:b],
                           None if u is None else u[:b], inp.temperature, inp.mode)
 
-    # each step: a bounded sample of the batch (<= ~0.2 s of CPU time)
-    b = 1
-    while b < inp.B:
+    # each step: a sample of the first b sequences, b as large as lets all
+    # --steps steps finish within REF_BUDGET_S (b >= 1; with b = 1 and a very
+    # large --steps the count is cut to what the budget holds, and the line
+    # reports the steps actually timed)
+    def step_time(bb, reps=3):
         t0 = time.perf_counter()
-        step(min(inp.B, b * 2))
-        if time.perf_counter() - t0 > 0.2:
+        for _ in range(reps):
+            step(bb)
+        return (time.perf_counter() - t0) / reps
+
+    K = max(args.steps, 1)
+    b, tb = 1, step_time(1)
+    while b < inp.B:
+        nb = min(inp.B, b * 2)
+        tn = step_time(nb)
+        if tn * K > REF_BUDGET_S:
             break
-        b = min(inp.B, b * 2)
+        b, tb = nb, tn
+    steps = K if tb * K <= REF_BUDGET_S else max(1, int(REF_BUDGET_S / tb))
     for _ in range(max(args.warmup, 1)):
         step(b)
-    steps = args.steps if args.steps <= 2000 else 2000
     t0 = time.perf_counter()
     for _ in range(steps):
         step(b)
