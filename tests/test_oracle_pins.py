@@ -800,3 +800,37 @@ def test_scd_data_errors_and_arguments():
     for bad in (-0.1, 1.5, float("nan")):
         with pytest.raises(ValueError):
             oracle.scd_verify_ref(t, a, x, u, 1.0, alpha=bad)
+
+
+def test_rejection_cut_random_shapes_against_the_library_quantile():
+    """Random prompt sizes, cut fractions and score patterns (ties, signed
+    zeros, wide ranges) against numpy's linear quantile and the kept-set
+    definition."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=150, deadline=None)
+    @hyp.given(st.integers(1, 300), st.floats(0.0, 1.0), st.integers(0, 2**31 - 1),
+               st.sampled_from(["normal", "ties", "wide"]))
+    def check(N, alpha, seed, kind):
+        rng = np.random.default_rng(seed)
+        if kind == "normal":
+            s = rng.standard_normal((3, N))
+        elif kind == "ties":
+            s = rng.integers(-2, 3, (3, N)).astype(np.float64)
+            s[s == 0] = np.where(rng.random((s == 0).sum()) < 0.5, -0.0, 0.0)
+        else:
+            s = rng.standard_normal((3, N)) * 10.0 ** rng.integers(-30, 30, (3, N))
+        s = s.astype(np.float32)
+        res = oracle.rejection_cut_ref(s, alpha)
+        assert res["status"] == 0
+        for g in range(3):
+            row = s[g].astype(np.float64)
+            q = np.quantile(row, alpha)
+            assert res["r_cut"][g] == pytest.approx(q, rel=1e-12, abs=1e-300)
+            n = res["n_accepted"][g]
+            kept = res["accepted"][g, :n]
+            np.testing.assert_array_equal(kept, np.flatnonzero(row >= res["r_cut"][g]))
+            assert n >= 1 and np.all(res["accepted"][g, n:] == -1)
+
+    check()
