@@ -45,8 +45,10 @@
  *   - greedy: argmax of the raw logit values (bf16 widens exactly), lowest
  *     index on ties.
  *   - contrastive target ([SCD] "Speculative Contrastive Decoding"; the
- *     formula was lost from the page: contrastive_row is "parity unpinned",
- *     only its two limits and the verify step around it are pinned):
+ *     formula was lost from the page, so contrastive_row follows the plain
+ *     reading below, pinned by the tests to its verbal definition built
+ *     from library softmaxes, to its two limits and by the verify step's
+ *     output law):
  *     contrastive decoding's log p_e - log p_a over the plausible head
  *     { p_e >= alpha * max p_e }, normalised there (contrastive_row); the
  *     amateur supplies the draft distribution q and its row K enters only

@@ -690,9 +690,10 @@ def test_rejection_cut_data_errors_and_shapes():
 # Decoding]", section Speculative Contrastive Decoding): speculative sampling
 # against the contrastive target P_n of expert and amateur, bonus from P_n.
 # The page lost P_n's formula; the oracle reads it as contrastive decoding's
-# log p_e - log p_a over the plausible head {p_e >= alpha max p_e}.  That
-# formula stays unpinned by the pages; the pins below fix its two limits and
-# the exactness of the verify step against it.
+# log p_e - log p_a over the plausible head {p_e >= alpha max p_e}.  The
+# pins below fix that reading to its verbal definition (library softmaxes,
+# interior alpha, several temperatures), its two limits and the exactness of
+# the verify step against it.
 # --------------------------------------------------------------------------
 def _scd_inputs(B, K, V, seed, T=1.0, amateur_zero=False):
     rng = np.random.default_rng(seed)
@@ -781,6 +782,94 @@ def test_scd_emitted_token_follows_the_contrastive_target():
     assert sel2.sum() > 2000 and counts2[~head2].sum() == 0
     _, pval2 = stats.chisquare(counts2[head2], sel2.sum() * pn2[head2])
     assert pval2 > 1e-3, pval2
+
+
+def _contrastive_by_definition(t_row, a_row, T, alpha):
+    """P_n of one position built from its verbal definition with library
+    softmaxes only: the plausible head is every token whose expert
+    probability softmax(t/T) is at least alpha times the expert's largest
+    probability, and P_n is the ratio expert / amateur of the two softmaxes
+    (log p_e - log p_a) renormalised over that head, zero elsewhere.
+    Returns (P_n, head, closest relative distance of a token to the cut)."""
+    pe = torch.softmax(torch.from_numpy(t_row.astype(np.float64)) / T, 0)
+    pa = torch.softmax(torch.from_numpy(a_row.astype(np.float64)) / T, 0)
+    cut = alpha * pe.max()
+    head = pe >= cut
+    ratio = torch.where(head, pe / pa, torch.zeros_like(pe))
+    pn = ratio / ratio.sum()
+    gap = ((pe[pe > 0] - cut).abs() / cut).min().item()
+    return pn.numpy(), head.numpy(), gap
+
+
+@pytest.mark.parametrize("T,alpha", [(0.7, 0.1), (0.7, 0.5), (0.05, 0.3), (0.05, 0.8),
+                                     (1.6, 0.25), (1.0, 0.05)])
+def test_scd_contrastive_target_from_its_definition(T, alpha):
+    """P_n away from both limits (0 < alpha < 1, T != 1), against the
+    definition itself rather than the oracle's own threshold M + T ln(alpha):
+    the oracle's P_n,i at EVERY token j (sequence j proposes x_i = j at each
+    position i, so p_at[j, i] = P_n,i(j)) equals the renormalised ratio of
+    two library softmaxes on the head {p_e >= alpha max p_e} to 1e-12, and is
+    exactly zero off the head.  A head threshold without the temperature
+    (M + ln alpha), a contrast without it (exp(t - a)) or an unrenormalised
+    ratio would each fail here at these (T, alpha)."""
+    V, K = 64, 3
+    rng = np.random.default_rng(int(1000 * T + 100 * alpha))
+    t = (rng.standard_normal((K + 1, V)) * 1.5).astype(np.float32)
+    a = (t + rng.standard_normal((K + 1, V)) * 0.8).astype(np.float32)
+    # a cluster of near-maximal logits in every row, so that the head at the
+    # small temperatures holds several tokens (spacings 0.004-0.05 logits)
+    for i in range(K + 1):
+        top = t[i].max()
+        idx = rng.choice(V, size=6, replace=False)
+        t[i, idx] = top - np.cumsum(rng.uniform(0.004, 0.05, 6)).astype(np.float32)
+    t[:, 7] = -np.inf  # a masked token: never in the head
+    x = np.repeat(np.arange(V, dtype=np.int32)[:, None], K, 1)
+    u = np.zeros((V, K + 1), np.float32)
+    res = oracle.scd_verify_ref(np.broadcast_to(t, (V, K + 1, V)), np.broadcast_to(a, (V, K + 1, V)),
+                                x, u, T, alpha, want_debug=True)
+    assert res["status"] == 0
+    sizes = []
+    for i in range(K):
+        pn, head, gap = _contrastive_by_definition(t[i], a[i], T, alpha)
+        assert gap > 1e-9, "a token sits on the head's cut: the test would not decide it"
+        got = res["p_at"][:, i]
+        np.testing.assert_allclose(got, pn, rtol=1e-10, atol=1e-12, err_msg=f"position {i}")
+        np.testing.assert_array_equal(got > 0, head, err_msg=f"support at position {i}")
+        assert not head[7]
+        sizes.append(int(head.sum()))
+    # the cut is active and not trivial: neither every finite token nor only the argmax
+    assert max(sizes) > 1 and min(sizes) < V - 1, sizes
+
+
+def test_scd_contrastive_bonus_draw_from_its_definition():
+    """The bonus token (all K accepted) comes from P_n at position K, the
+    definition's law on rows K of expert and amateur: with uniforms on a
+    grid, the emitted token is the inverse CDF of that law, pinned here as
+    numpy's searchsorted on the cumulative definition (u away from steps)."""
+    V, K, T, alpha = 24, 1, 0.7, 0.2
+    rng = np.random.default_rng(77)
+    t = (rng.standard_normal((K + 1, V)) * 1.2).astype(np.float32)
+    a = (t + rng.standard_normal((K + 1, V)) * 0.7).astype(np.float32)
+    pn0, head0, _ = _contrastive_by_definition(t[0], a[0], T, alpha)
+    pnK, headK, gap = _contrastive_by_definition(t[K], a[K], T, alpha)
+    assert gap > 1e-9 and 1 < headK.sum() < V
+    # x_0 = the head token with the largest P_n,0 / q_0: accepted for every u
+    qa = torch.softmax(torch.from_numpy(a[0].astype(np.float64)) / T, 0).numpy()
+    x0 = int(np.argmax(np.where(head0, pn0 / qa, -1.0)))
+    assert pn0[x0] >= qa[x0]
+    cdf = np.cumsum(pnK)
+    us = np.linspace(0.0, 0.999, 400).astype(np.float32)
+    keep = np.min(np.abs(us[:, None].astype(np.float64) - cdf[None, :]), 1) > 1e-6
+    us = us[keep]
+    n = us.size
+    u = np.zeros((n, K + 1), np.float32)
+    u[:, K] = us
+    res = oracle.scd_verify_ref(np.broadcast_to(t, (n, K + 1, V)), np.broadcast_to(a, (n, K + 1, V)),
+                                np.full((n, K), x0, np.int32), u, T, alpha)
+    assert np.all(res["accepted_len"] == K)
+    want = np.searchsorted(cdf, us.astype(np.float64), side="right")
+    np.testing.assert_array_equal(res["out_tokens"][:, K], want)
+    assert set(np.unique(want)) == set(np.flatnonzero(headK))
 
 
 def test_scd_data_errors_and_arguments():
