@@ -2,16 +2,19 @@
 """Benchmark of the verify step (one JSON line on stdout).
 
 A step is one spec_verify call over one batch of the workload.  The default
-workload is the greedy blockwise-parallel verify of 64 sequences x 8 draft
-positions over a 32000-token bf16 vocabulary; ``--workload`` picks another of
-the seeded workloads (draft_verify_acceptance_gb300.workloads.WORKLOADS).
+workload is the largest one: the best-of-N-scale sampling verify of 1024
+candidate sequences x 4 draft positions over a 32000-token bf16 vocabulary
+(590 MB of logits per call); ``--workload`` picks another of the seeded
+workloads (draft_verify_acceptance_gb300.workloads.WORKLOADS).  Every other
+workload gets a complete line of its own under "workloads".
 
 Device timing: the inputs are resident in HBM as R rotating copies whose total
 exceeds twice the L2 size, so every step reads its logits from DRAM; K steps
 are captured in CUDA graphs and timed with CUDA events on the launching
-stream, bracketed by barrier + synchronize.  The metric is verified draft
-positions per second (B*K per step, summed over ranks) over the max time of
-all ranks.  ``e2e`` times the public call with pinned HOST tensors (copies
+stream, bracketed by barrier + synchronize; one untimed replay is enqueued
+just before the start event so the graphs' launch latency is not timed.  The
+metric is verified draft positions per second (B*K per step, summed over
+ranks) over the max time of all ranks.  ``e2e`` times the public call with pinned HOST tensors (copies
 host->device, the kernel, device->host of the outputs, per step).
 
 ``--impl reference`` times the CPU oracle on the machine's host cores instead
@@ -31,7 +34,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "greedy_bf16_B64_K8_V32000"
+DEFAULT_WORKLOAD = "best_of_n_bf16_B1024_K4_V32000"
 METRIC = "verified draft positions/sec (B*K/s)"
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
@@ -41,7 +44,7 @@ REF_BUDGET_S = 150.0  # the reference arm's timed CPU work
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -235,9 +238,10 @@ def kernel_plan(inp):
     return "norm_stream_kernel", 2
 
 
-def committed_traffic(workload, kernel):
+def committed_traffic(workload, kernel, key="dram_bytes_per_launch"):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, only
-    if it was taken on that kernel's current sources."""
+    if it was taken on that kernel's current sources (`key`
+    "call_dram_bytes": all kernels of one verify call)."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             d = json.load(f)
@@ -246,61 +250,192 @@ def committed_traffic(workload, kernel):
     e = d.get(workload)
     if not e or e.get("kernel") != kernel or e.get("source_hash") != kernel_source_hash(kernel):
         return None
-    return e.get("dram_bytes_per_launch")
+    return e.get(key)
 
 
 # --------------------------------------------------------------------------
 # native arm
 # --------------------------------------------------------------------------
-def device_time(binding, inp, steps, warmup, dev, l2_bytes, mode=None):
-    """Prepare `steps` launches that rotate over R device copies of the inputs
-    (R * bytes > 2x L2), warm up, and capture them in CUDA graphs.  Returns
-    (R, algorithmic bytes per launch, stream, graphs to replay, two events,
-    the output tensors).  `mode` overrides the inputs' mode (early exit)."""
+def rotating_copies(nbytes, l2_bytes):
+    """How many input copies a timed loop rotates over so that every launch
+    reads its inputs from DRAM: their total exceeds twice the L2 size."""
+    return min(64, max(2, math.ceil(2 * l2_bytes / max(nbytes, 1)) + 1))
+
+
+class GraphTimer:
+    """`steps` calls of `launch(k)` captured in CUDA graphs of at most 1000
+    launches each, replayed on `stream` and timed there with CUDA events.
+
+    Every run first enqueues one untimed replay, then the start event, the
+    timed graphs and the stop event: the timed graphs are submitted while the
+    GPU is still busy with the untimed replay, so the start event fires when
+    that replay ends and the graphs' launch latency stays outside the
+    measured interval, whatever `steps` is."""
+
+    def __init__(self, launch, steps, warmup, stream, dev):
+        import torch
+        self.stream, self.dev, self.steps = stream, dev, steps
+        with torch.cuda.stream(stream):
+            for w in range(max(warmup, 3)):
+                launch(w)
+        stream.synchronize()
+        G = min(steps, 1000)
+        graphs = {}
+        for n in sorted({G, steps % G} - {0}):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(n):
+                    launch(k)
+            graphs[n] = g
+        self.graphs = graphs
+        self.plan = [graphs[G]] * (steps // G) + ([graphs[steps % G]] if steps % G else [])
+        self.warm = graphs[G]
+        with torch.cuda.stream(stream):  # one untimed replay of each graph
+            for g in graphs.values():
+                g.replay()
+        torch.cuda.synchronize(dev)
+        self.e0 = torch.cuda.Event(enable_timing=True)
+        self.e1 = torch.cuda.Event(enable_timing=True)
+
+    def run(self, before_start=None):
+        """Enqueue the untimed replay, `before_start()` (work that must run
+        after it but outside the timed interval), the start event, the timed
+        graphs and the stop event; the caller synchronizes."""
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.warm.replay()
+            if before_start is not None:
+                before_start()
+            self.e0.record(self.stream)
+            for g in self.plan:
+                g.replay()
+            self.e1.record(self.stream)
+
+    def seconds(self):
+        return self.e0.elapsed_time(self.e1) / 1e3
+
+    def per_launch(self):
+        import torch
+        torch.cuda.synchronize(self.dev)
+        self.run()
+        torch.cuda.synchronize(self.dev)
+        return self.seconds() / self.steps
+
+
+def device_setup(binding, inp, dev, l2_bytes, mode=None):
+    """R rotating device copies of the inputs (R * bytes > 2x L2), the outputs,
+    a zero-filled workspace, a stream, and launch(k): one verify call on copy
+    k mod R.  `mode` overrides the inputs' mode (early exit)."""
     import torch
     mode = inp.mode if mode is None else mode
-    nbytes = inp.algorithmic_bytes()
-    R = max(2, math.ceil(2 * l2_bytes / max(nbytes, 1)) + 1)
-    R = min(R, 64)
-    copies = []
-    for r in range(R):
-        copies.append(tuple(None if t is None else t.to(dev) for t in
-                            (inp.target, inp.draft, inp.tokens, inp.uniforms)))
+    R = rotating_copies(inp.algorithmic_bytes(), l2_bytes)
+    copies = [tuple(None if t is None else t.to(dev) for t in
+                    (inp.target, inp.draft, inp.tokens, inp.uniforms)) for _ in range(R)]
     acc = torch.empty(inp.B, dtype=torch.int32, device=dev)
     out = torch.empty((inp.B, inp.K + 1), dtype=torch.int32, device=dev)
     dt = binding.DTYPE_BF16 if inp.target.dtype == torch.bfloat16 else binding.DTYPE_F32
-    ws = torch.zeros(binding.workspace_size(inp.B, inp.K, inp.V, dt, inp.mode),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.zeros(binding.workspace_size(inp.B, inp.K, inp.V, dt, mode), dtype=torch.uint8,
+                     device=dev)
     stream = torch.cuda.Stream(dev)
 
-    def launch(r):
-        c = copies[r % R]
+    def launch(k):
+        c = copies[k % R]
         binding.verify(c[0], c[1], c[2], c[3], inp.temperature, mode, stream=stream,
                        workspace=ws, out=(acc, out))
 
+    return R, stream, launch, (acc, out)
+
+
+def roofline(inp, nbytes, sec_per_call, peak, peak_kind, workload):
+    kernel, launches = kernel_plan(inp)
+    achieved = nbytes / sec_per_call / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind,
+            "traffic": committed_traffic(workload, kernel),
+            "call_traffic": committed_traffic(workload, kernel, key="call_dram_bytes"),
+            "algorithmic_bytes_per_launch": nbytes, "kernel": kernel,
+            "kernels_per_call": launches}
+
+
+def e2e_record(binding, inp, stream, world, steps):
+    """The public call on pinned HOST tensors: every step copies the inputs
+    host -> device, verifies, and copies the outputs back (the binding
+    synchronizes the stream before returning)."""
+    import torch
+    host = [None if t is None else t.pin_memory() for t in
+            (inp.target, inp.draft, inp.tokens, inp.uniforms)]
     with torch.cuda.stream(stream):
-        for w in range(max(warmup, 3)):
-            launch(w)
-    stream.synchronize()
-    G = min(steps, 1000)
-    graphs = []
-    for n in sorted({G, steps % G} - {0}):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(n):
-                launch(k)
-        graphs.append((n, g))
-    plan = [graphs[-1][1]] * (steps // G) if G else []
-    if steps % G:
-        plan.append([g for n, g in graphs if n == steps % G][0])
-    # one untimed replay of each graph
-    with torch.cuda.stream(stream):
-        for _, g in graphs:
-            g.replay()
+        for _ in range(3):
+            binding.verify(*host, inp.temperature, inp.mode, stream=stream)
+        barrier(world)
+        h0 = time.perf_counter()
+        for _ in range(steps):
+            binding.verify(*host, inp.temperature, inp.mode, stream=stream)
+        h1 = time.perf_counter()
+    sec = max_over_ranks(h1 - h0, world)
+    h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
+    d2h = inp.B * 4 + inp.B * (inp.K + 1) * 4
+    return {"value": inp.B * inp.K * world * steps / sec, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "path": "binding.verify on pinned host tensors (H2D, kernel, D2H, sync)"}
+
+
+def parity_record(binding, inp, dev):
+    """One spec_verify_ex call on the whole batch against the oracle on the
+    same input bytes: how many sequences are bit-equal, how many each
+    boundary category excludes (the oracle's flags in double: the ratio
+    band, the CDF band, a residual mass below the band; and the kernel's own
+    flags), the largest error of p_i(x_i) and q_i(x_i), the mean accepted
+    length and the empirical acceptance rate of each draft position."""
+    import numpy as np
+    import torch
+    import oracle
+    from draft_verify_acceptance_gb300 import workloads as W
+    mv = lambda t: None if t is None else t.to(dev)
+    res = binding.verify_ex(mv(inp.target), mv(inp.draft), mv(inp.tokens), mv(inp.uniforms),
+                            inp.temperature, inp.mode)
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    return R, nbytes, stream, plan, e0, e1, (acc, out)
+    ref = oracle.verify_ref(W.as_numpy_logits(inp.target), W.as_numpy_logits(inp.draft),
+                            inp.tokens.numpy(), None if inp.uniforms is None else inp.uniforms.numpy(),
+                            inp.temperature, inp.mode, want_debug=True)
+    n = res["accepted_len"].cpu().numpy()
+    out = res["out_tokens"].cpu().numpy()
+    fl = ref["flags"]
+    ok = fl == 0
+    equal = (n == ref["accepted_len"]) & (out == ref["out_tokens"]).all(1)
+    rec = {"sequences": int(inp.B), "compared": int(ok.sum()),
+           "bit_equal": int((equal & ok).sum()), "mismatched": int((~equal & ok).sum()),
+           "flagged": {"ratio_band": int(((fl & oracle.FLAG_RATIO) != 0).sum()),
+                       "cdf_band": int(((fl & oracle.FLAG_CDF) != 0).sum()),
+                       "tiny_residual": int(((fl & oracle.FLAG_TINY_RESIDUAL) != 0).sum()),
+                       "any": int((~ok).sum()),
+                       "flagged_but_equal": int((equal & ~ok).sum())},
+           "kernel_flagged": int((res["flags"].cpu().numpy() != 0).sum()),
+           "status": int(res["status"].item()), "oracle_status": int(ref["status"])}
+    if inp.mode == W.MODE_SAMPLE and inp.K > 0:
+        rec["p_at_max_abs_err"] = float(np.abs(res["p_at"].cpu().numpy() - ref["p_at"]).max())
+        rec["q_at_max_abs_err"] = float(np.abs(res["q_at"].cpu().numpy() - ref["q_at"]).max())
+        rec["tolerance"] = 2e-3 if inp.dtype_name == "bf16" else 1e-5
+    per_pos = []
+    for i in range(inp.K):
+        reached = int((n >= i).sum())
+        per_pos.append(round(float((n > i).sum()) / reached, 4) if reached else None)
+    acc = {"mean_accepted_len": float(n.mean()) if n.size else 0.0, "per_position": per_pos}
+    return rec, acc
+
+
+def cpu_baselines(inp, budget_s):
+    """The oracle as it stands on all host cores and on one core."""
+    import oracle
+    allc = cpu_baseline(inp, budget_s)
+    nmax = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        one = cpu_baseline(inp, budget_s)
+    finally:
+        oracle.set_threads(nmax)
+    allc["single_core"] = {"value": one["value"], "cores": 1, "sample": one["sample"]}
+    return allc
 
 
 def run_native(args, rank, world, local):
@@ -312,9 +447,9 @@ def run_native(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 * 2**20)
     inp = W.workload(args.workload, seed=shard_seed(0, rank))
-    R, nbytes, stream, plan, e0, e1, acc_out = device_time(binding, inp, args.steps, args.warmup,
-                                                           dev, l2)
-    acc_out[0].fill_(-1)
+    nbytes = inp.algorithmic_bytes()
+    R, stream, launch, (acc, out) = device_setup(binding, inp, dev, l2)
+    timer = GraphTimer(launch, args.steps, args.warmup, stream, dev)
 
     clocks = ClockSampler(local)
     if rank == 0:
@@ -322,52 +457,35 @@ def run_native(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):  # graphs replay on the current stream
-        e0.record(stream)
-        for g in plan:
-            g.replay()
-        e1.record(stream)
+    # the outputs are cleared after the untimed replay, so the check below
+    # sees what the timed graphs wrote
+    timer.run(before_start=lambda: acc.fill_(-1))
     torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
     barrier(world)
-    # the replayed graphs wrote real outputs (guards against timing an empty graph)
-    n_host = acc_out[0].cpu()
+    n_host = acc.cpu()
     if not (int(n_host.min()) >= 0 and int(n_host.max()) <= inp.K):
         raise RuntimeError("timed launches did not produce valid outputs")
     clk = clocks.stop(t0, t1) if rank == 0 else None
-    sec = e0.elapsed_time(e1) / 1e3
+    sec = timer.seconds()
     sec_max = max_over_ranks(sec, world)
+    del timer, launch
+    torch.cuda.empty_cache()
 
     positions = inp.B * inp.K
     value = positions * world * args.steps / sec_max
-    per_launch = sec / args.steps
     peak, peak_kind = hbm_peak()
-    achieved = nbytes / per_launch / 1e9
+    e2e = e2e_record(binding, inp, stream, world, max(20, min(args.steps, 200)))
 
-    # end to end through the public call with pinned host tensors
-    e2e_steps = max(20, min(args.steps, 500))
-    host = [None if t is None else t.pin_memory() for t in
-            (inp.target, inp.draft, inp.tokens, inp.uniforms)]
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            binding.verify(*host, inp.temperature, inp.mode, stream=stream)
-        barrier(world)
-        h0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            binding.verify(*host, inp.temperature, inp.mode, stream=stream)
-        h1 = time.perf_counter()
-    e2e_sec = max_over_ranks(h1 - h0, world)
-    h2d = sum(t.numel() * t.element_size() for t in host if t is not None)
-    d2h = inp.B * 4 + inp.B * (inp.K + 1) * 4
-
-    extras = None
-    cpu = None
+    extras = cpu = parity = accept = None
     if rank == 0 and world == 1 and not args.no_extras:
-        extras = per_workload_table(binding, args.workload, dev, l2, peak)
-        cpu = cpu_baseline(inp)
+        parity, accept = parity_record(binding, inp, dev)
+        cpu = cpu_baselines(inp, 5.0)
+        extras = per_workload_table(binding, args.workload, dev, l2, peak, peak_kind)
 
     if rank != 0:
         return
+    kernel, launches = kernel_plan(inp)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec_max * 1e3 / args.steps,
@@ -380,45 +498,53 @@ def run_native(args, rank, world, local):
                    "parallelism": f"replicas x{world}",
                    "l2": f"{R} rotating input copies of {nbytes / 1e6:.1f} MB (> 2x L2 of "
                          f"{l2 / 2**20:.0f} MiB)",
-                   "timing": "CUDA graphs of <=1000 launches, CUDA events on the launch stream"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": committed_traffic(args.workload, kernel_plan(inp)[0]),
-                     "algorithmic_bytes_per_launch": nbytes,
-                     "kernel": kernel_plan(inp)[0]},
-        "e2e": {"value": positions * world * e2e_steps / e2e_sec, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "binding.verify on pinned host tensors (H2D, kernel, D2H, sync)"},
-        "gpu_launches": args.steps * kernel_plan(inp)[1],
+                   "timing": "CUDA graphs of <=1000 launches after one untimed replay, "
+                             "CUDA events on the launch stream"},
+        "roofline": roofline(inp, nbytes, sec_max / args.steps, peak, peak_kind, args.workload),
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "parity": parity,
+        "acceptance": accept,
         "workloads": extras,
     }
     print(json.dumps(line))
 
 
-def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
-    """Device throughput of every other workload (same timing method)."""
+def workload_record(binding, inp, dev, l2, peak, peak_kind, steps=500, cpu_budget=3.0):
+    """The complete line of one seeded workload: device time per call
+    (graph-replayed, inputs rotating over copies > 2x L2), its roofline, the
+    end-to-end figure, the oracle at all cores and at one core, and the
+    parity and acceptance record."""
+    import torch
+    R, stream, launch, _ = device_setup(binding, inp, dev, l2)
+    sec = GraphTimer(launch, steps, 5, stream, dev).per_launch()
+    del launch
+    torch.cuda.empty_cache()
+    nbytes = inp.algorithmic_bytes()
+    rec = {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec,
+           "roofline": roofline(inp, nbytes, sec, peak, peak_kind, inp.name),
+           "e2e": e2e_record(binding, inp, stream, 1, 20)}
+    rec["parity"], rec["acceptance"] = parity_record(binding, inp, dev)
+    rec["cpu_baseline"] = cpu_baselines(inp, cpu_budget)
+    return rec, sec
+
+
+def per_workload_table(binding, skip, dev, l2, peak, peak_kind, steps=500):
+    """A complete line for every other workload, and the variant lines
+    (early exit, draft sampler, contrastive verify, rejection cut)."""
     import torch
     from draft_verify_acceptance_gb300 import workloads as W
     table = {}
     for name in W.WORKLOADS:
-        if name == skip:
-            continue
         inp = W.workload(name)
-        R, nbytes, stream, plan, e0, e1, _ = device_time(binding, inp, steps, 5, dev, l2)
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for g in plan:
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        sec = e0.elapsed_time(e1) / 1e3 / steps
-        table[name] = {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec,
-                       "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
-                       "algorithmic_bytes": nbytes}
-        del plan
+        if name != skip:
+            table[name], sec = workload_record(binding, inp, dev, l2, peak, peak_kind, steps)
+        else:
+            R, stream, launch, _ = device_setup(binding, inp, dev, l2)
+            sec = GraphTimer(launch, steps, 5, stream, dev).per_launch()
+            del launch
         torch.cuda.empty_cache()
         if inp.mode == W.MODE_SAMPLE and inp.K > 0:
             table[name + "+early_exit"] = early_exit_line(binding, inp, steps, dev, l2, peak, sec)
@@ -433,8 +559,11 @@ def per_workload_table(binding, skip, dev, l2, peak, steps=3000):
 def scd_line(binding, name, spec, steps, dev, l2, peak):
     """Speculative contrastive decoding's verify step (bytes: every expert
     and amateur row read once, the tokens, the uniforms and the outputs),
-    graph-replayed over rotating input copies > 2x L2 like the rest."""
+    graph-replayed over rotating input copies > 2x L2 like the rest; the
+    oracle's time on a sample of the batch beside it."""
+    import numpy as np
     import torch
+    import oracle
     from draft_verify_acceptance_gb300 import workloads as W
     spec = dict(spec)
     alpha = spec.pop("alpha")
@@ -442,7 +571,7 @@ def scd_line(binding, name, spec, steps, dev, l2, peak):
     B, K, V = inp.B, inp.K, inp.V
     es = inp.target.element_size()
     nbytes = 2 * B * (K + 1) * V * es + B * K * 4 + B * (K + 1) * 4 + B * 4 + B * (K + 1) * 4
-    R = min(64, max(2, math.ceil(2 * l2 / max(nbytes, 1)) + 1))
+    R = rotating_copies(nbytes, l2)
     copies = [tuple(t.to(dev) for t in (inp.target, inp.draft, inp.tokens, inp.uniforms))
               for _ in range(R)]
     dt = binding.DTYPE_BF16 if inp.target.dtype == torch.bfloat16 else binding.DTYPE_F32
@@ -457,30 +586,34 @@ def scd_line(binding, name, spec, steps, dev, l2, peak):
         binding.verify_scd(c[0], c[1], c[2], c[3], inp.temperature, alpha, stream=stream,
                            workspace=ws, out=out)
 
-    with torch.cuda.stream(stream):
-        for r in range(3):
-            launch(r)
-        stream.synchronize()
-        n = min(steps, 1000)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(n):
-                launch(k)
-        g.replay()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    sec = e0.elapsed_time(e1) / 1e3 / n
+    sec = GraphTimer(launch, steps, 3, stream, dev).per_launch()
     mean_n = float(out[0].float().mean().item())
-    del g, copies
+    del launch, copies
     torch.cuda.empty_cache()
-    return {"us_per_step": sec * 1e6, "positions_per_s": B * K / sec, "bytes": nbytes,
-            "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
-            "kernel": "scd_row_kernel", "mean_accepted_len": mean_n,
-            "traffic": committed_traffic(inp.name, "scd_row_kernel")}
+    # parity of the last call's batch against the oracle, and the oracle's time
+    t = W.as_numpy_logits(inp.target)
+    a = W.as_numpy_logits(inp.draft)
+    c0 = time.perf_counter()
+    ref = oracle.scd_verify_ref(t, a, inp.tokens.numpy(), inp.uniforms.numpy(), inp.temperature,
+                                alpha, want_debug=True)
+    cpu_sec = time.perf_counter() - c0
+    ok = ref["flags"] == 0
+    n = out[0].cpu().numpy()
+    o = out[1].cpu().numpy()
+    equal = (n == ref["accepted_len"]) & (o == ref["out_tokens"]).all(1)
+    achieved = nbytes / sec / 1e9
+    return {"us_per_step": sec * 1e6, "positions_per_s": B * K / sec,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": nbytes,
+                         "kernel": "scd_row_kernel",
+                         "traffic": committed_traffic(inp.name, "scd_row_kernel")},
+            "mean_accepted_len": mean_n,
+            "parity": {"sequences": B, "compared": int(ok.sum()),
+                       "bit_equal": int((equal & ok).sum()),
+                       "mismatched": int((~equal & ok).sum()), "flagged": int((~ok).sum())},
+            "cpu_baseline": {"value": B * K / cpu_sec, "unit": UNIT,
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"the whole batch ({B} sequences), once"}}
 
 
 def rejection_cut_line(binding, name, spec, steps, dev, l2, peak):
@@ -488,44 +621,40 @@ def rejection_cut_line(binding, name, spec, steps, dev, l2, peak):
     scores read, the kept-index rows, r_cut and the counts written),
     graph-replayed over rotating score copies > 2x L2; the oracle's time on
     the same batch beside it."""
+    import numpy as np
     import torch
+    import oracle
     from draft_verify_acceptance_gb300 import workloads as W
     G, N, alpha = spec["G"], spec["N"], spec["alpha"]
     scores = W.make_scores(G, N, kind=spec["kind"], seed=0)
     nbytes = G * N * 4 * 2 + G * (8 + 4)
-    R = min(64, max(2, math.ceil(2 * l2 / max(nbytes, 1)) + 1))
+    R = rotating_copies(nbytes, l2)
     copies = [scores.to(dev) for _ in range(R)]
     out = (torch.empty(G, dtype=torch.float64, device=dev),
            torch.empty(G, dtype=torch.int32, device=dev),
            torch.empty((G, N), dtype=torch.int32, device=dev))
     stream = torch.cuda.Stream(dev)
-    with torch.cuda.stream(stream):
-        for r in range(3):
-            binding.rejection_cut(copies[r % R], alpha, stream=stream, out=out)
-        stream.synchronize()
-        n = min(steps, 1000)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(n):
-                binding.rejection_cut(copies[k % R], alpha, stream=stream, out=out)
-        g.replay()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    sec = e0.elapsed_time(e1) / 1e3 / n
-    del g, copies
+
+    def launch(k):
+        binding.rejection_cut(copies[k % R], alpha, stream=stream, out=out)
+
+    sec = GraphTimer(launch, steps, 3, stream, dev).per_launch()
+    del launch, copies
     torch.cuda.empty_cache()
-    import oracle
     t0 = time.perf_counter()
-    oracle.rejection_cut_ref(scores.numpy(), alpha)
+    ref = oracle.rejection_cut_ref(scores.numpy(), alpha)
     cpu_sec = time.perf_counter() - t0
-    return {"us_per_step": sec * 1e6, "scores_per_s": G * N / sec, "bytes": nbytes,
-            "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak,
-            "kernel": "cut_warp_kernel" if N <= 1024 else "cut_block_kernel",
-            "traffic": committed_traffic(name, "cut_warp_kernel") if N <= 1024 else None,
+    same = (np.array_equal(out[0].cpu().numpy(), ref["r_cut"])
+            and np.array_equal(out[1].cpu().numpy(), ref["n_accepted"])
+            and np.array_equal(out[2].cpu().numpy(), ref["accepted"]))
+    kernel = "cut_warp_kernel" if N <= 1024 else "cut_block_kernel"
+    achieved = nbytes / sec / 1e9
+    return {"us_per_step": sec * 1e6, "scores_per_s": G * N / sec,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": nbytes,
+                         "kernel": kernel,
+                         "traffic": committed_traffic(name, kernel)},
+            "parity": {"prompts": G, "bit_equal": bool(same)},
             "cpu_baseline": {"value": G * N / cpu_sec, "unit": "scores/s",
                              "cores": oracle.max_threads(), "kind": "oracle",
                              "sample": f"the whole batch ({G} x {N}), once"}}
@@ -537,7 +666,7 @@ def draft_sample_line(binding, inp, steps, dev, l2, peak):
     import torch
     s = inp.draft.element_size()
     nbytes = inp.B * inp.K * inp.V * s + inp.B * inp.K * 4 * 3
-    R = min(64, max(2, math.ceil(2 * l2 / max(nbytes, 1)) + 1))
+    R = rotating_copies(nbytes, l2)
     copies = [inp.draft.to(dev) for _ in range(R)]
     u = inp.uniforms[:, :inp.K].contiguous().to(dev)
     dt = binding.DTYPE_BF16 if inp.draft.dtype == torch.bfloat16 else binding.DTYPE_F32
@@ -546,26 +675,13 @@ def draft_sample_line(binding, inp, steps, dev, l2, peak):
     stream = torch.cuda.Stream(dev)
     out = (torch.empty(u.shape, dtype=torch.int32, device=dev),
            torch.empty(u.shape, dtype=torch.float32, device=dev))
-    with torch.cuda.stream(stream):
-        for r in range(3):
-            binding.draft_sample(copies[r % R], u, inp.temperature, stream=stream, workspace=ws,
-                                 out=out)
-        stream.synchronize()
-        n = min(steps, 1000)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(n):
-                binding.draft_sample(copies[k % R], u, inp.temperature, stream=stream, workspace=ws,
-                                     out=out)
-        g.replay()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    sec = e0.elapsed_time(e1) / 1e3 / n
-    del g, copies
+
+    def launch(k):
+        binding.draft_sample(copies[k % R], u, inp.temperature, stream=stream, workspace=ws,
+                             out=out)
+
+    sec = GraphTimer(launch, steps, 3, stream, dev).per_launch()
+    del launch, copies
     torch.cuda.empty_cache()
     return {"us_per_step": sec * 1e6, "rows_per_s": inp.B * inp.K / sec, "bytes": nbytes,
             "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak}
@@ -576,21 +692,14 @@ def early_exit_line(binding, inp, steps, dev, l2, peak, parallel_sec):
     position 0's row pairs, plus every row when some sequence accepted x_0
     (then the full verify runs too); the outputs equal sampling mode's."""
     import torch
-    R, nbytes, stream, plan, e0, e1, (acc, _) = device_time(
-        binding, inp, steps, 5, dev, l2, mode=binding.MODE_SAMPLE_EARLY_EXIT)
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for g in plan:
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    sec = e0.elapsed_time(e1) / 1e3 / steps
+    R, stream, launch, (acc, _) = device_setup(binding, inp, dev, l2,
+                                               mode=binding.MODE_SAMPLE_EARLY_EXIT)
+    sec = GraphTimer(launch, steps, 5, stream, dev).per_launch()
     s = inp.target.element_size()
     first = 2 * inp.B * inp.V * s + inp.B * 4 + inp.B * 4 + inp.B * (inp.K + 2) * 4
     full_ran = bool((acc > 0).any().item())  # the last replayed call's outputs
-    read = first + (nbytes if full_ran else 0)
-    del plan
+    read = first + (inp.algorithmic_bytes() if full_ran else 0)
+    del launch
     torch.cuda.empty_cache()
     return {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec,
             "bytes_read": read, "GB_per_s": read / sec / 1e9, "frac_hbm": read / sec / 1e9 / peak,
@@ -607,14 +716,15 @@ def cpu_baseline(inp, budget_s=10.0):
     x = inp.tokens.numpy()
     u = None if inp.uniforms is None else inp.uniforms.numpy()
     B = inp.B
-    # a bounded sample: the first b sequences, doubled until one call takes >= 0.5 s
+    # a bounded sample: the first b sequences, doubled until one call takes
+    # >= budget_s / 20
     b = max(1, min(B, 4))
     while True:
         t0 = time.perf_counter()
         oracle.verify_ref(t[:b], None if d is None else d[:b], x[:b], None if u is None else u[:b],
                           inp.temperature, inp.mode)
         dt = time.perf_counter() - t0
-        if dt >= 0.5 or b == B:
+        if dt >= budget_s / 20 or b == B:
             break
         b = min(B, b * 2)
     reps, total, t0 = 0, 0.0, time.perf_counter()
