@@ -56,9 +56,9 @@ long long sample_tiles(long long nvec, int cluster);
 cudaError_t launch_greedy(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
-// The fused sampling kernel (16-byte aligned rows of at most
-// kFusedMaxVec vectors); launch_sample dispatches to it.
-constexpr long long kFusedMaxVec = 65536;
+// The fused sampling kernel (16-byte aligned rows of at most kFusedMaxVec
+// vectors: one draw segment); launch_sample dispatches to it.
+constexpr long long kFusedMaxVec = 4096;
 cudaError_t sample_fused_prepare();
 cudaError_t launch_sample_fused(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 

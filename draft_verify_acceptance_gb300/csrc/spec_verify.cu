@@ -124,8 +124,11 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
 
   const long long rows = static_cast<long long>(B) * (K + 1);
   if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
-  const bool fused = a.vec && rowbytes / 16 <= specv::kFusedMaxVec;
-  if (sample && !fused) {  // limits of the streaming sampler
+  // aligned rows go to the fused or the two-kernel sampler; the streaming
+  // sampler takes the rest
+  const bool streaming = !a.vec || (rowbytes / 16 > specv::kFusedMaxVec &&
+                                    specv::sample_2p_cluster(rowbytes / 16) == 0);
+  if (sample && streaming) {  // limits of the streaming sampler
     const long long nvec = a.vec ? rowbytes / 16 : V;
     const int C = specv::sample_cluster_size(V, esz);
     if (specv::sample_tiles(nvec, C) > specv::kMaxTiles) return SPEC_ERR_UNSUPPORTED;

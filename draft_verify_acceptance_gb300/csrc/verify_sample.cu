@@ -409,7 +409,6 @@ cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream
     if (a.early_exit && a.K >= 1 && C > 0) return launch_sample_early_exit(a, dev, C, stream);
     if (nvec <= kFusedSeg) return launch_sample_fused(a, dev, stream);
     if (C > 0) return launch_sample_2p(a, dev, C, stream);
-    if (nvec <= kFusedMaxVec) return launch_sample_fused(a, dev, stream);
   }
   // unaligned rows, or rows too long for the fused kernel: the streaming
   // kernel below

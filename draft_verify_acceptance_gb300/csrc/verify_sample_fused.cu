@@ -64,7 +64,7 @@ constexpr int kDecWarp = kCW + 2;
 constexpr int kThreadsF = (kCW + 3) * 32;
 constexpr int kLs = 2 * kCT;                // vectors per row per stage (16 KiB)
 constexpr int kStageVec = 2 * kLs;          // vectors per stage (32 KiB)
-constexpr int kStagesF = 5;
+constexpr int kStagesF = 6;
 constexpr int kMaxEntries = static_cast<int>(kFusedMaxVec / 32);  // 32-vector runs per row
 constexpr int kScratch = 512;               // partials per decision window
 constexpr int kPartBuf = 16;                // unit ends the consumers may run ahead
