@@ -174,6 +174,8 @@ KERNEL_SOURCES = {
     "norm_stream_kernel": ["verify_sample_2p.cu", "sample_common.cuh", "device_common.cuh",
                            "launch.h"],
     "sample_kernel": ["verify_sample.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
+    "seq_sample_kernel": ["verify_sample_seq.cu", "sample_common.cuh", "device_common.cuh",
+                          "launch.h"],
     "cut_warp_kernel": ["rejection_cut.cu", "launch.h"],
     "scd_row_kernel": ["verify_scd.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
 }
@@ -222,10 +224,11 @@ def kernel_source_hash(kernel, read=None):
 def kernel_plan(inp):
     """(dominant kernel, kernel launches per verify call) for these inputs: the
     library's dispatch (src: launch_greedy / launch_sample) restated --
-    greedy: one greedy_kernel; sampling with 16-byte aligned rows of at most
-    4096 vectors: one fused_sample_kernel; longer aligned rows (up to the
-    two-kernel sampler's limit): norm_stream_kernel then
-    decide_sample_kernel; otherwise the streaming sample_kernel."""
+    greedy: one greedy_kernel; sampling with 16-byte aligned rows: at most
+    one sequence per SM (152) whose 2K+1 rows fit 192 KiB: one
+    seq_sample_kernel; else rows of at most 4096 vectors: one
+    fused_sample_kernel; longer rows: norm_stream_kernel then
+    decide_sample_kernel; unaligned rows: the streaming sample_kernel."""
     from draft_verify_acceptance_gb300 import workloads as W
     if inp.mode == W.MODE_GREEDY:
         return "greedy_kernel", 1
@@ -233,6 +236,8 @@ def kernel_plan(inp):
     if (inp.V * esz) % 16 != 0:
         return "sample_kernel", 1
     nvec = inp.V * esz // 16
+    if inp.B <= 152 and (2 * inp.K + 1) * nvec * 16 <= 192 * 1024:
+        return "seq_sample_kernel", 1
     if nvec <= 4096:
         return "fused_sample_kernel", 1
     return "norm_stream_kernel", 2

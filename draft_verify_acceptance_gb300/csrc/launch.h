@@ -62,6 +62,13 @@ constexpr long long kFusedMaxVec = 4096;
 cudaError_t sample_fused_prepare();
 cudaError_t launch_sample_fused(const VerifyArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
+// Small batches: one CTA per sequence with its K+1 target rows and K draft
+// rows staged in shared memory (at most kSeqMaxBytes of them); no workspace.
+constexpr int kSeqMaxBytes = 192 * 1024;
+long long seq_sample_bytes(int K, long long nvec);
+cudaError_t seq_sample_prepare();
+cudaError_t launch_sample_seq(const VerifyArgs& a, cudaStream_t stream);
+
 // The two-kernel sampler (normaliser stream, then decide and draw with one
 // cluster per sequence) for rows whose draw spans several draw segments.
 int sample_2p_cluster(long long nvec);

@@ -30,6 +30,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     if (e == cudaSuccess) e = greedy_occupancy(&d.greedy_ctas_per_sm);
     if (e == cudaSuccess) e = sample_prepare();
     if (e == cudaSuccess) e = sample_fused_prepare();
+    if (e == cudaSuccess) e = seq_sample_prepare();
     if (e == cudaSuccess) e = sample_2p_prepare(&d);
     if (e == cudaSuccess) e = row_sample_prepare();
     if (e == cudaSuccess) e = scd_prepare();

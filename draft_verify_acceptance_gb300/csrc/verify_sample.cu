@@ -405,6 +405,11 @@ cudaError_t launch_sample(const VerifyArgs& a, const DeviceInfo& dev, cudaStream
     // longer rows: the two-kernel sampler, whose per-sequence clusters finish
     // the last draws sooner (measured: the fused kernel takes 59 / 106 us on
     // the 128256-row bf16 and 152064-row fp32 batches, against 47 / 65)
+    // a batch of at most one sequence per SM whose sequences fit one CTA's
+    // shared memory: one CTA per sequence, everything on chip (early-exit
+    // mode included: every row is read anyway, and the outputs are the same)
+    if (a.B <= dev.sm_count && seq_sample_bytes(a.K, nvec) <= kSeqMaxBytes)
+      return launch_sample_seq(a, stream);
     const int C = sample_2p_cluster(nvec);
     if (a.early_exit && a.K >= 1 && C > 0) return launch_sample_early_exit(a, dev, C, stream);
     if (nvec <= kFusedSeg) return launch_sample_fused(a, dev, stream);

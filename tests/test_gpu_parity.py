@@ -115,6 +115,15 @@ SAMPLE_CASES = [
     ("f32_V2", 64, 3, 2, torch.float32, 1.0, dict(target_std=1.0, draft_noise=1.0)),
     ("bf16_V3", 64, 2, 3, torch.bfloat16, 1.5, dict(target_std=1.0, draft_noise=1.0)),
     ("bf16_V4096_T0.05", 16, 4, 4096, torch.bfloat16, 0.05, dict(target_std=1.0, draft_noise=0.1)),
+    # more sequences than SMs: the fused kernel (the cases above with at most
+    # one sequence per SM and short rows take the small-batch kernel)
+    ("f32_V1000_B200_fused", 200, 4, 1000, torch.float32, 1.0, dict(target_std=3.0, draft_noise=0.5)),
+    ("bf16_V4096_B160_T0.05_fused", 160, 4, 4096, torch.bfloat16, 0.05,
+     dict(target_std=1.0, draft_noise=0.1)),
+    ("f32_Kmax_B160_fused", 160, 64, 300, torch.float32, 1.0, dict(target_std=1.0, draft_noise=0.2)),
+    ("f32_K0_B300_fused", 300, 0, 5000, torch.float32, 1.0, dict(target_std=3.0)),
+    # a small batch whose 2K+1 rows just fit the small-batch kernel's 192 KiB
+    ("bf16_V10912_K4_smem_limit", 8, 4, 10912, torch.bfloat16, 1.0, dict(target_std=4.0, draft_noise=1.0)),
 ]
 
 

@@ -69,17 +69,35 @@ def test_reward_scores_recipe():
 
 
 @pytest.mark.parametrize("name", list(W.WORKLOADS))
-def test_kernel_plan_matches_the_dispatch_rule(name):
+@pytest.mark.parametrize("B", [2, None, 152, 153, 400])
+def test_kernel_plan_matches_the_dispatch_rule(name, B):
+    """The bench's restatement of launch_sample's dispatch: at most one
+    sequence per SM (152) whose 2K+1 rows fit 192 KiB -> the small-batch
+    kernel; else rows of at most 4096 vectors -> the fused kernel; longer rows
+    -> the two-kernel sampler."""
+    import types
     spec = W.WORKLOADS[name]
-    inp = W.workload(name, B=2)
+    inp = types.SimpleNamespace(B=spec["B"] if B is None else B, K=spec["K"], V=spec["V"],
+                                mode=spec["mode"],
+                                dtype_name="bf16" if spec["dtype"] == torch.bfloat16 else "f32")
     kernel, launches = bench.kernel_plan(inp)
     if spec["mode"] == W.MODE_GREEDY:
         assert (kernel, launches) == ("greedy_kernel", 1)
     else:
         esz = 2 if spec["dtype"] == torch.bfloat16 else 4
         nvec = spec["V"] * esz // 16
-        want = ("fused_sample_kernel", 1) if nvec <= 4096 else ("norm_stream_kernel", 2)
+        K = spec["K"]
+        if inp.B <= 152 and (2 * K + 1) * nvec * 16 <= 192 * 1024:
+            want = ("seq_sample_kernel", 1)
+        elif nvec <= 4096:
+            want = ("fused_sample_kernel", 1)
+        else:
+            want = ("norm_stream_kernel", 2)
         assert (kernel, launches) == want
+    if name == "tiny_sample_f32_B4_K4_V1000" and inp.B <= 152:
+        assert kernel == "seq_sample_kernel"
+    if name == "best_of_n_bf16_B1024_K4_V32000":
+        assert kernel == "fused_sample_kernel"
 
 
 def test_algorithmic_bytes_count_every_row_once():
