@@ -39,7 +39,8 @@ FLAG_RATIO = 1
 FLAG_CDF = 2
 
 EXPORTS = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size", "spec_status_string",
-           "spec_verify_static", "spec_draft_sample", "spec_rejection_cut", "spec_verify_scd")
+           "spec_verify_static", "spec_draft_sample", "spec_rejection_cut", "spec_verify_scd",
+           "spec_set_wait_limit")
 
 
 class SpecVerifyError(RuntimeError):
@@ -70,6 +71,8 @@ def _load():
                                     P, P, P, P]
     lib.spec_rejection_cut.restype = I
     lib.spec_rejection_cut.argtypes = [P, I, I, ctypes.c_double, P, P, P, P, P]
+    lib.spec_set_wait_limit.restype = I
+    lib.spec_set_wait_limit.argtypes = [ctypes.c_uint]
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [I]
     return lib
@@ -82,6 +85,13 @@ _ws_cache = {}
 
 def status_string(code: int) -> str:
     return _lib.spec_status_string(int(code)).decode()
+
+
+def set_wait_limit(microseconds: int) -> None:
+    """Bound (microseconds; 0 = the default 2 s) on a kernel's waits for work
+    of other thread blocks; past it the kernel stops and reports
+    DEVICE_WAIT_TIMEOUT in the status word (spec_set_wait_limit)."""
+    _lib.spec_set_wait_limit(int(microseconds))
 
 
 def workspace_size(B: int, K: int, V: int, dtype: int, mode: int) -> int:

@@ -302,6 +302,13 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t pari
   return false;
 }
 
+// The GPU's nanosecond clock (%globaltimer), for waits bounded in time.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // ---- cluster barrier, split -----------------------------------------------
 // Every thread of every CTA of the cluster arrives early and waits just
 // before its first access to another CTA's shared memory: that access must

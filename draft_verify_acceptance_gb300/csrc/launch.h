@@ -34,6 +34,9 @@ struct VerifyArgs {
   bool early_exit = false;     // sampling: verify position 0 first (SPEC_MODE_SAMPLE_EARLY_EXIT)
   float* p_emit = nullptr;     // [B] or null: p_n of the token emitted at position n
                                // (fused and two-kernel samplers; the draft sampler's q(x))
+  // Longest a kernel waits, without progress, on work of other warps or
+  // thread blocks before it gives up and reports SPEC_DEVICE_WAIT_TIMEOUT.
+  unsigned long long wait_ns = 2000000000ull;
 };
 
 // Per-device facts gathered once.

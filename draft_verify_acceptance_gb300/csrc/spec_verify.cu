@@ -1,6 +1,7 @@
 // spec_verify.cu -- the C ABI of libspecverify.so (declared in
 // include/spec_verify.h): argument validation on the host, one-time per-
 // device set-up, and dispatch to the greedy or sampling kernel.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -46,6 +47,11 @@ cudaError_t device_info(int device, DeviceInfo* out) {
 namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Bound on a kernel's waits for work of other warps or thread blocks
+// (spec_set_wait_limit); read at every launch.
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
 }  // namespace
 
@@ -122,6 +128,7 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
   a.early_exit = mode == SPEC_MODE_SAMPLE_EARLY_EXIT;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
 
   const long long rows = static_cast<long long>(B) * (K + 1);
   if (rows * specv::kMaxCluster > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
@@ -203,6 +210,7 @@ spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R
   a.flags = nullptr;
   a.status = device_status;
   a.p_emit = q_at;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   const specv::WorkspaceLayout lay = specv::workspace_layout(R, 0, V, esz);
   a.seq = reinterpret_cast<specv::SeqState*>(static_cast<char*>(workspace) + lay.seq);
   a.slots = static_cast<char*>(workspace) + lay.units;
@@ -275,6 +283,12 @@ spec_status_t spec_verify_scd(const void* target_logits, const void* amateur_log
   const cudaError_t e =
       specv::launch_scd(a, amateur_logits, L, C, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_set_wait_limit(unsigned int microseconds) {
+  g_wait_ns.store(microseconds == 0 ? kDefaultWaitNs : 1000ull * microseconds,
+                  std::memory_order_relaxed);
+  return SPEC_OK;
 }
 
 const char* spec_status_string(int status) {

@@ -71,7 +71,6 @@ constexpr int kPartBuf = 16;                // unit ends the consumers may run a
 constexpr int kUQ = 64;                     // producer -> arrivals: units issued
 constexpr int kBatch = 8;                   // unit ends the arrival warp takes at once
 constexpr int kRounds = (64 + 1 + 31) / 32; // rows per lane in a decision (K <= 64)
-constexpr unsigned int kMaxIdle = 1u << 22;
 // Decisions -> producer draw requests.  At most 2 are issued and unfinished
 // (two run-mass tables); the decision warp posts at most one request per
 // sequence it owns.
@@ -145,6 +144,35 @@ __device__ __forceinline__ void set_abort(FusedShared& sh, const VerifyArgs& a) 
   if (a.status) atomicOr(a.status, kWaitTimeout);
 }
 
+// Polling for work of other warps or thread blocks, bounded in time:
+// expired() answers true once the caller has polled for longer than the
+// call's wait limit since its last progress().
+struct WaitClock {
+  unsigned long long since = 0, limit;
+  __device__ explicit WaitClock(unsigned long long l) : limit(l) {}
+  __device__ __forceinline__ void progress() { since = 0; }
+  __device__ __forceinline__ bool expired() {
+    const unsigned long long t = global_ns();
+    if (since == 0) {
+      since = t;
+      return false;
+    }
+    return t - since > limit;
+  }
+};
+
+// Waits for phase `parity` of `bar`, the thread sleeping in hardware between
+// polls.  False when the CTA aborts or the wait limit passes first.
+__device__ __forceinline__ bool wait_phase(unsigned long long* bar, uint32_t parity,
+                                           const FusedShared& sh, unsigned long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait_sleep(bar, parity, 5000u)) {
+    if (vld(sh.abort_flag) || global_ns() - t0 > limit) return false;
+  }
+  return true;
+}
+
 // Position in the ring of stages: slot q, the parity of the slot's current
 // round, and whether the ring has wrapped once (32-bit, no division).
 struct RingPos {
@@ -165,9 +193,10 @@ struct RingPos {
 
 // The producer may refill slot p.q once the consumers released its previous
 // round.
-__device__ __forceinline__ bool acquire_slot(FusedShared& sh, const RingPos& p) {
+__device__ __forceinline__ bool acquire_slot(FusedShared& sh, const RingPos& p,
+                                             unsigned long long limit) {
   if (!p.wrapped) return true;
-  return mbar_wait_sleep(&sh.empty[p.q], p.ph ^ 1u);
+  return wait_phase(&sh.empty[p.q], p.ph ^ 1u, sh, limit);
 }
 
 // Copies vectors [off, off+len) of target row `trow` (and of draft row
@@ -203,14 +232,14 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
   // one unit is claimed ahead of its use
   unsigned long long next = atomicAdd(&ctl->next_task, 1ull);
   bool have_next = true;
-  unsigned int idle = 0;
+  WaitClock idle(a.wait_ns);
 
   while (true) {
     if (vld(sh.abort_flag)) break;
     if (in_unit) {  // finish the current unit first
       const int per = cdrow ? kLs : kStageVec;
       const int len = min(per, cend - cnext);
-      if (!acquire_slot(sh, pos)) {
+      if (!acquire_slot(sh, pos, a.wait_ns)) {
         ok = false;
         break;
       }
@@ -225,7 +254,7 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
       pos.advance();
       cnext += len;
       if (cnext >= cend) in_unit = false;
-      idle = 0;
+      idle.progress();
       continue;
     }
     const long long posted = vld(sh.req_posted);
@@ -240,7 +269,7 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
       const uint4* drow = j.residual ? D + (static_cast<size_t>(j.b) * K + j.n) * nvec : nullptr;
       for (int off = 0; off < nvec; off += per) {
         const int len = min(per, nvec - off);
-        if (!acquire_slot(sh, pos)) {
+        if (!acquire_slot(sh, pos, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -261,7 +290,7 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
       }
       if (!ok) break;
       ++taken;
-      idle = 0;
+      idle.progress();
       continue;
     }
     if (have_next) {  // start the unit claimed ahead
@@ -278,7 +307,7 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
         continue;
       }
       if (units - vld(sh.units_folded) >= kUQ) {  // the arrival warp is kUQ units behind
-        if (++idle > kMaxIdle) {
+        if (idle.expired()) {
           ok = false;
           break;
         }
@@ -311,11 +340,11 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
       vst(sh.units_issued, ++units);
       next = atomicAdd(&ctl->next_task, 1ull);  // the next unit, claimed ahead
       have_next = true;
-      idle = 0;
+      idle.progress();
       continue;
     }
     if (exhausted && !want_draw && vld(sh.exit_flag)) {
-      if (acquire_slot(sh, pos)) {
+      if (acquire_slot(sh, pos, a.wait_ns)) {
         sh.info[pos.q].kind = kExit;
         mbar_arrive(&sh.full[pos.q]);
         ++k;
@@ -325,15 +354,17 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
       }
       break;
     }
-    if (++idle > kMaxIdle) {
+    if (idle.expired()) {
       ok = false;
       break;
     }
     __nanosleep(128);
   }
-  if (!ok) {
-    set_abort(sh, a);
-    // let the copies already issued land before the CTA can exit
+  if (!ok) set_abort(sh, a);
+  if (!ok || vld(sh.abort_flag)) {
+    // an early exit (this warp's or another's): the consumers may leave
+    // without reading the stages still in flight, so the copies already
+    // issued must land before the CTA can exit
     for (long long kk = (k > kStagesF ? k - kStagesF : 0); kk < k; ++kk)
       mbar_wait_sleep(&sh.full[kk % kStagesF], static_cast<uint32_t>((kk / kStagesF) & 1));
   }
@@ -356,7 +387,7 @@ __device__ __forceinline__ void run_consumers(const VerifyArgs& a, FusedShared& 
   bool ok = true;
   for (;; pos.advance()) {
     const int q = pos.q;
-    if (!mbar_wait_sleep(&sh.full[q], pos.ph)) {
+    if (!wait_phase(&sh.full[q], pos.ph, sh, a.wait_ns)) {
       ok = false;  // the producer stopped (abort) or a copy never landed
       break;
     }
@@ -400,7 +431,7 @@ __device__ __forceinline__ void run_consumers(const VerifyArgs& a, FusedShared& 
         const unsigned int buf = u % kPartBuf;
         if (lane == 0) {
           if (u >= kPartBuf &&
-              !mbar_wait_sleep(&sh.part_free[buf], ((u / kPartBuf) - 1u) & 1u))
+              !wait_phase(&sh.part_free[buf], ((u / kPartBuf) - 1u) & 1u, sh, a.wait_ns))
             ok = false;
           sh.part[buf][warp] = make_float4(mt, zt, md, zd);
           mbar_arrive(&sh.part_full[buf]);
@@ -487,7 +518,7 @@ __device__ __forceinline__ void run_arrivals(const VerifyArgs& a, const FusedGeo
   Partial* partials = static_cast<Partial*>(a.partials);
   long long u = 0;
   bool ok = true;
-  unsigned int idle = 0;
+  WaitClock idle(a.wait_ns);
   while (true) {
     if (vld(sh.abort_flag)) break;
     const long long issued = vld(sh.units_issued);
@@ -502,14 +533,14 @@ __device__ __forceinline__ void run_arrivals(const VerifyArgs& a, const FusedGeo
       if (u < issued) {  // wait for the next unit end
         int got = 0;
         if (lane == 0)
-          got = mbar_wait_sleep(&sh.part_full[u % kPartBuf], static_cast<uint32_t>((u / kPartBuf) & 1)) ? 1 : 0;
+          got = wait_phase(&sh.part_full[u % kPartBuf], static_cast<uint32_t>((u / kPartBuf) & 1), sh, a.wait_ns) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
           break;
         }
         nb = 1;
       } else {  // nothing issued yet
-        if (++idle > kMaxIdle) {
+        if (idle.expired()) {
           ok = false;
           break;
         }
@@ -517,7 +548,7 @@ __device__ __forceinline__ void run_arrivals(const VerifyArgs& a, const FusedGeo
         continue;
       }
     }
-    idle = 0;
+    idle.progress();
     __syncwarp();
     // fold each ready unit (lanes 0..15 hold its 16 warp values); lane j keeps unit u+j
     Partial mine{-INFINITY, 0.f, -INFINITY, 0.f};
@@ -772,7 +803,7 @@ __device__ __forceinline__ void run_decisions(const VerifyArgs& a, const FusedGe
   long long posted = 0, finished = 0;
   int nb = blockIdx.x;  // the next sequence this CTA owns
   bool ok = true;
-  unsigned int idle = 0;
+  WaitClock idle(a.wait_ns);
   while (nb < g.B || finished < posted) {
     if (vld(sh.abort_flag)) break;
     // the oldest outstanding draw is reduced: finish it (frees its table)
@@ -799,7 +830,7 @@ __device__ __forceinline__ void run_decisions(const VerifyArgs& a, const FusedGe
         vst(sh.draws_finished, finished);
         if (redo) vst(sh.req_posted, posted);
       }
-      idle = 0;
+      idle.progress();
       continue;
     }
     // the next owned sequence complete: decide it and request its draw
@@ -821,10 +852,10 @@ __device__ __forceinline__ void run_decisions(const VerifyArgs& a, const FusedGe
       }
       ++posted;
       nb += gridDim.x;
-      idle = 0;
+      idle.progress();
       continue;
     }
-    if (++idle > kMaxIdle) {
+    if (idle.expired()) {
       ok = false;
       break;
     }

@@ -76,8 +76,11 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
 #define SPEC_DATA_TOKEN_RANGE 1      /* a draft token outside [0, V) (clamped) */
 #define SPEC_DATA_NONFINITE_LOGIT 2  /* NaN or +inf logit, or a row with no finite entry */
 #define SPEC_DATA_UNIFORM_RANGE 4    /* a uniform outside [0, 1) or NaN */
-/* Not a data error: a kernel's bounded wait for its own bulk copies gave up
- * (outputs of that call are unspecified).  Never expected in normal use. */
+/* Not a data error: one of a kernel's bounded waits -- for its own bulk
+ * copies, or for work that other thread blocks of the same launch publish --
+ * gave up (see spec_set_wait_limit).  The outputs of that call are then
+ * unspecified and its workspace must be zero-filled again before reuse.
+ * Never expected in normal use. */
 #define SPEC_DEVICE_WAIT_TIMEOUT 8
 #define SPEC_DATA_NONFINITE_SCORE 16 /* spec_rejection_cut: a NaN or infinite score */
 
@@ -325,6 +328,20 @@ SPEC_API spec_status_t spec_rejection_cut(const float* scores, int G, int N, dou
 
 /* A short, static, human-readable description of a return code. */
 SPEC_API const char* spec_status_string(int status);
+
+/*
+ * spec_set_wait_limit -- bound on how long a kernel of this library waits,
+ * without progress, for work that other warps or thread blocks of the same
+ * launch publish (the sampling kernel for rows of at most 4096 16-byte
+ * vectors decides each sequence on one thread block once the blocks that
+ * streamed its rows have counted them).  Past the bound the kernel stops
+ * early, ORs SPEC_DEVICE_WAIT_TIMEOUT into the device status word and leaves
+ * that call's outputs unspecified, instead of waiting any longer.  The
+ * limit applies to launches queued after the call, process-wide and on every
+ * device.  microseconds == 0 restores the default of 2 s.  No counterpart on
+ * the pages: this is the library's failure detection.  Always SPEC_OK.
+ */
+SPEC_API spec_status_t spec_set_wait_limit(unsigned int microseconds);
 
 #ifdef __cplusplus
 }

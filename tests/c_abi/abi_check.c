@@ -55,6 +55,9 @@ int main(void) {
   CHECK(14, strcmp(spec_status_string(SPEC_OK), "ok") == 0);
   for (int c = SPEC_OK; c <= SPEC_ERR_SCRATCH_LIMIT; ++c)
     CHECK(15, spec_status_string(c) != NULL && spec_status_string(c)[0] != '\0');
+  /* the wait bound: set, and back to the default */
+  CHECK(16, spec_set_wait_limit(5000u) == SPEC_OK);
+  CHECK(17, spec_set_wait_limit(0u) == SPEC_OK);
   printf("abi_check: all checks passed\n");
   return 0;
 }

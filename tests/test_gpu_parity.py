@@ -35,18 +35,71 @@ def _dev(t):
     return None if t is None else t.to("cuda")
 
 
-def run_gpu(lib, inp, **kw):
-    res = lib.verify_ex(_dev(inp.target), _dev(inp.draft), _dev(inp.tokens), _dev(inp.uniforms),
-                        inp.temperature, inp.mode, **kw)
-    torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in res.items()}
+# Canary guards: every output, the status word and the workspace sit inside a
+# larger buffer whose GUARD bytes on each side hold the byte CANARY; after the
+# call every guard byte must still hold it (an out-of-range write by any
+# kernel shows up here), and the workspace body must be back to all zeros.
+GUARD = 256
+CANARY = 0xA5
+
+
+class Guarded:
+    def __init__(self, shape, dtype, fill=None):
+        self.shape, self.dtype = tuple(shape), dtype
+        self.nbytes = int(np.prod(self.shape, dtype=np.int64)) * torch.empty(0, dtype=dtype).element_size()
+        self.buf = torch.full((self.nbytes + 2 * GUARD,), CANARY, dtype=torch.uint8, device="cuda")
+        if fill is not None:
+            self.buf[GUARD:GUARD + self.nbytes].fill_(fill)
+        self.body = self.buf[GUARD:GUARD + self.nbytes].view(dtype).view(self.shape)
+
+    def ptr(self):
+        import ctypes
+        return ctypes.c_void_p(self.buf.data_ptr() + GUARD)
+
+    def guards_intact(self):
+        g = torch.cat([self.buf[:GUARD], self.buf[GUARD + self.nbytes:]])
+        return bool((g == CANARY).all().item())
 
 
 def run_gpu_mode(lib, inp, mode):
-    res = lib.verify_ex(_dev(inp.target), _dev(inp.draft), _dev(inp.tokens), _dev(inp.uniforms),
-                        inp.temperature, mode)
+    """spec_verify_ex through the C ABI with every output, the status word and
+    the workspace in guarded buffers; fails if a guard byte changed or the
+    workspace is not left zero-filled."""
+    import ctypes
+    mode = lib._mode(mode)
+    B, K, V = inp.B, inp.K, inp.V
+    dt = lib.DTYPE_BF16 if inp.target.dtype == torch.bfloat16 else lib.DTYPE_F32
+    dev = [_dev(t) for t in (inp.target, inp.draft, inp.tokens, inp.uniforms)]
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    acc = Guarded((B,), torch.int32)
+    out = Guarded((B, K + 1), torch.int32)
+    p_at = Guarded((B, K), torch.float32, 0)
+    q_at = Guarded((B, K), torch.float32, 0)
+    flags = Guarded((B,), torch.int32, 0)
+    status = Guarded((1,), torch.int32, 0)
+    wsb = lib.workspace_size(B, K, V, dt, mode)
+    ws = Guarded((wsb,), torch.uint8, 0)
+    sample = mode != lib.MODE_GREEDY
+    stream = torch.cuda.current_stream()
+    rc = lib._lib.spec_verify_ex(
+        ptr(dev[0]), ptr(dev[1]) if sample else None, ptr(dev[2]) if K > 0 else None,
+        ptr(dev[3]) if sample else None, B, K, V, dt, float(inp.temperature), mode,
+        acc.ptr(), out.ptr(), ws.ptr(), wsb, ctypes.c_void_p(stream.cuda_stream),
+        p_at.ptr(), q_at.ptr(), flags.ptr(), status.ptr())
+    assert rc == lib.OK, lib.status_string(rc)
     torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in res.items()}
+    for name, g in (("accepted_len", acc), ("out_tokens", out), ("p_at", p_at), ("q_at", q_at),
+                    ("flags", flags), ("status", status), ("workspace", ws)):
+        assert g.guards_intact(), f"a kernel wrote outside {name}"
+    if int(status.body.item()) == 0:
+        assert int(ws.body.count_nonzero().item()) == 0, "workspace not left zero-filled"
+    return {"accepted_len": acc.body.cpu().numpy(), "out_tokens": out.body.cpu().numpy(),
+            "p_at": p_at.body.cpu().numpy(), "q_at": q_at.body.cpu().numpy(),
+            "flags": flags.body.cpu().numpy(), "status": status.body.cpu().numpy()}
+
+
+def run_gpu(lib, inp):
+    return run_gpu_mode(lib, inp, inp.mode)
 
 
 def run_oracle(inp):
@@ -291,6 +344,24 @@ def test_greedy_data_errors(lib):
     assert int(g["status"][0]) == ref["status"] == 3
 
 
+@pytest.mark.parametrize("shape", [(300, 4, 1000, torch.float32), (8, 4, 3000, torch.bfloat16),
+                                   (64, 8, 32000, torch.bfloat16)],
+                         ids=["fused", "small_batch", "greedy"])
+def test_bit_identical_over_100_runs(lib, shape):
+    """Races in the reductions or the arrival protocol would make repeated runs
+    on the same inputs differ: 100 runs must give identical outputs,
+    diagnostics included."""
+    B, K, V, dtype = shape
+    mode = W.MODE_GREEDY if V == 32000 else W.MODE_SAMPLE
+    inp = W.make_inputs(B, K, V, dtype=dtype, mode=mode, temperature=0.9, target_std=4.0,
+                        draft_noise=1.0, seed=17)
+    first = run_gpu(lib, inp)
+    for _ in range(99):
+        cur = run_gpu(lib, inp)
+        for k in first:
+            assert np.array_equal(cur[k], first[k]), k
+
+
 def test_deterministic_and_workspace_left_zero(lib):
     inp = W.make_inputs(64, 5, 50000, dtype=torch.bfloat16, temperature=0.9, target_std=4.0,
                         draft_noise=1.0, seed=13)
@@ -298,7 +369,7 @@ def test_deterministic_and_workspace_left_zero(lib):
     nbytes = lib.workspace_size(64, 5, 50000, lib.DTYPE_BF16, lib.MODE_SAMPLE)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     first = None
-    for _ in range(20):
+    for _ in range(100):
         acc, out = lib.verify(*dev, inp.temperature, "sample", workspace=ws)
         torch.cuda.synchronize()
         cur = (acc.cpu().numpy(), out.cpu().numpy())

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(binding):
     names = _declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
                           "spec_status_string", "spec_verify_static", "spec_draft_sample",
-                          "spec_rejection_cut", "spec_verify_scd"}
+                          "spec_rejection_cut", "spec_verify_scd", "spec_set_wait_limit"}
     assert set(names) == set(binding.EXPORTS)
     lib = ctypes.CDLL(binding.LIB_PATH)
     for n in names:
