@@ -33,24 +33,39 @@ def _deps():
     return files
 
 
-def _stale():
-    if not os.path.exists(LIB):
+LIB_DEBUG = os.path.join(HERE, "libspecverify_debug.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+
+
+def _stale(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if any source is newer than it."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile and link the library if any source is newer than it.
+
+    debug=True builds the test variant libspecverify_debug.so with
+    -DSPEC_DEBUG: the kernels' index checks skip an out-of-range global access
+    and report SPEC_DEBUG_BOUNDS in the status word instead of faulting.  The
+    same optional flag SPEC_NVTX (environment variable SPEC_NVTX=1 at build
+    time) wraps every entry point in an NVTX range."""
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     common = [nvcc, "-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xptxas", "-v",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
+    if debug:
+        common.append("-DSPEC_DEBUG")
+    if os.environ.get("SPEC_NVTX") == "1":
+        common.append("-DSPEC_NVTX")
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         r = subprocess.run(common + ["-c", os.path.join(CSRC, src), "-o", obj],
                            capture_output=True, text=True)
         if r.returncode != 0:
@@ -59,18 +74,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(bdir, "ptxas.log"), "w") as f:
         for _, log in results:
             f.write(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     r = subprocess.run([nvcc, "-shared", *ARCH, "-o", tmp] + [o for o, _ in results],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print(open(os.path.join(BUILD, "ptxas.log")).read())
-    return LIB
+        print(open(os.path.join(bdir, "ptxas.log")).read())
+    return lib
 
 
 if __name__ == "__main__":

@@ -22,6 +22,9 @@ constexpr int kWaitTimeout = 8;
 // for a short hardware-defined time); past it the kernel reports
 // kWaitTimeout instead of waiting forever.
 constexpr unsigned int kMaxPolls = 1u << 22;
+// Debug builds (-DSPEC_DEBUG) only: an index check on a kernel's global
+// access failed; the access was skipped (public SPEC_DEBUG_BOUNDS).
+constexpr int kDebugBounds = 32;
 // Per-sequence boundary flags (public SPEC_FLAG_*).
 constexpr uint32_t kFlagRatio = 1;
 constexpr uint32_t kFlagCdf = 2;
@@ -127,6 +130,22 @@ struct DivU64 {
 };
 
 #ifdef __CUDACC__
+
+// ---- debug-build index checks ----------------------------------------------
+// SPEC_IN(i, n, status): whether 0 <= i < n.  In a -DSPEC_DEBUG build a
+// failed check ORs kDebugBounds into the status word (when given) and the
+// caller skips the access instead of faulting; release builds compile every
+// check to `true`.
+#ifdef SPEC_DEBUG
+__device__ __forceinline__ bool spec_in(long long i, long long n, int32_t* status) {
+  if (i >= 0 && i < n) return true;
+  if (status) atomicOr(status, kDebugBounds);
+  return false;
+}
+#define SPEC_IN(i, n, status) ::specv::spec_in(static_cast<long long>(i), static_cast<long long>(n), (status))
+#else
+#define SPEC_IN(i, n, status) true
+#endif
 
 // ---- loads ---------------------------------------------------------------
 // 16-byte streaming load through the read-only path, no L1 allocation.

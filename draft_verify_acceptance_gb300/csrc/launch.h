@@ -6,6 +6,23 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+// Optional NVTX ranges around every entry point (build with -DSPEC_NVTX; the
+// NVTX3 headers are header-only and cost nothing without a profiler).
+#ifdef SPEC_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace specv {
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace specv
+#define SPEC_RANGE(name) ::specv::NvtxRange spec_nvtx_range_(name)
+#else
+#define SPEC_RANGE(name) \
+  do {                   \
+  } while (0)
+#endif
+
 namespace specv {
 
 struct SeqState;
@@ -31,6 +48,8 @@ struct VerifyArgs {
   void* partials;              // workspace: Partial per work unit (fused sampler); same
                                // region as `slots`
   void* ctl;                   // workspace: FusedCtl (work counters)
+  long long ws_units = 0;      // 16-byte slots in the `slots` / `partials` region (index checks
+                               // of debug builds)
   bool early_exit = false;     // sampling: verify position 0 first (SPEC_MODE_SAMPLE_EARLY_EXIT)
   float* p_emit = nullptr;     // [B] or null: p_n of the token emitted at position n
                                // (fused and two-kernel samplers; the draft sampler's q(x))

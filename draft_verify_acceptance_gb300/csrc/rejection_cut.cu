@@ -323,6 +323,7 @@ extern "C" {
 spec_status_t spec_rejection_cut(const float* scores, int G, int N, double alpha, double* r_cut,
                                  int32_t* n_accepted, int32_t* accepted, spec_stream_t stream,
                                  int32_t* device_status) {
+  SPEC_RANGE("spec_rejection_cut");
   if (G < 0 || N < 0 || !(alpha >= 0.0 && alpha <= 1.0)) return SPEC_ERR_INVALID_ARG;
   if (G == 0) return SPEC_OK;
   if (N < 1 || !scores || !r_cut || !n_accepted || !accepted) return SPEC_ERR_INVALID_ARG;

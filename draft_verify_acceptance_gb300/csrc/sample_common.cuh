@@ -349,6 +349,11 @@ __device__ __forceinline__ volatile int32_t* candidate_slot(const VerifyArgs& a,
 __device__ __forceinline__ void warp_arrive_and_finalize(const VerifyArgs& a, int b) {
   const int lane = threadIdx.x & 31;
   const int K = a.K, K1 = K + 1;
+  // (debug builds) the sequence and its K+1 candidate slots lie in the batch
+  // and the workspace
+  if (!(SPEC_IN(b, a.B, a.status) &&
+        SPEC_IN((static_cast<long long>(b) + 1) * K1 - 1, a.ws_units, a.status)))
+    return;
   int last = 0;
   if (lane == 0) last = arrive_last(a.seq, b, static_cast<unsigned int>(K1)) ? 1 : 0;
   last = __shfl_sync(0xffffffffu, last, 0);

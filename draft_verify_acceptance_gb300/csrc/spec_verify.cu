@@ -10,6 +10,7 @@
 #include "device_common.cuh"
 #include "launch.h"
 
+
 namespace specv {
 
 cudaError_t greedy_occupancy(int* ctas_per_sm);
@@ -72,6 +73,7 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
                              size_t workspace_bytes, spec_stream_t stream,
                              float* p_at_draft, float* q_at_draft, uint32_t* flags,
                              int32_t* device_status) {
+  SPEC_RANGE("spec_verify_ex");
   // ---- sizes, enums ------------------------------------------------------
   if (B < 0 || K < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
@@ -127,6 +129,7 @@ spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits
   a.slots = static_cast<char*>(workspace) + lay.units;
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
+  a.ws_units = static_cast<long long>((lay.ctl - lay.units) / 16);
   a.early_exit = mode == SPEC_MODE_SAMPLE_EARLY_EXIT;
   a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
 
@@ -160,6 +163,7 @@ spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R
                                 float temperature, int32_t* tokens, float* q_at, void* workspace,
                                 size_t workspace_bytes, spec_stream_t stream,
                                 int32_t* device_status) {
+  SPEC_RANGE("spec_draft_sample");
   if (R < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
   if (V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
@@ -216,6 +220,7 @@ spec_status_t spec_draft_sample(const void* logits, const float* uniforms, int R
   a.slots = static_cast<char*>(workspace) + lay.units;
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
+  a.ws_units = static_cast<long long>((lay.ctl - lay.units) / 16);
   const cudaError_t e = specv::launch_sample(a, info, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -226,6 +231,7 @@ spec_status_t spec_verify_scd(const void* target_logits, const void* amateur_log
                               int32_t* accepted_len, int32_t* out_tokens, void* workspace,
                               size_t workspace_bytes, spec_stream_t stream, float* p_at_draft,
                               float* q_at_draft, uint32_t* flags, int32_t* device_status) {
+  SPEC_RANGE("spec_verify_scd");
   if (B < 0 || K < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_INVALID_ARG;
   if (!(temperature > 0.f && std::isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
@@ -278,6 +284,7 @@ spec_status_t spec_verify_scd(const void* target_logits, const void* amateur_log
   a.slots = static_cast<char*>(workspace) + lay.units;
   a.partials = static_cast<char*>(workspace) + lay.units;
   a.ctl = static_cast<char*>(workspace) + lay.ctl;
+  a.ws_units = static_cast<long long>((lay.ctl - lay.units) / 16);
   // the head's log-threshold T ln(alpha), in double (alpha = 0: no cut)
   const double L = alpha > 0.0 ? static_cast<double>(temperature) * std::log(alpha) : -INFINITY;
   const cudaError_t e =

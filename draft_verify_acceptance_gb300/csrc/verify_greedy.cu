@@ -220,6 +220,7 @@ greedy_kernel(VerifyArgs a, int nvec, int S, DivU64 by_S, DivU64 by_K1, bool one
       }
       if (flags && a.status) atomicOr(a.status, flags);
       int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
+      if (!(SPEC_IN(b, a.B, a.status) && SPEC_IN(pos, K1, a.status))) return;
       out[pos] = bidx;  // x_i when it matches, g_n at the first mismatch
       const unsigned long long add = (1ull << 48) | (mism ? (1ull << pos) : 0ull);
       const unsigned long long now = atom_add_acq_rel_gpu(&a.seq[b].row_word, add) + add;
@@ -240,9 +241,11 @@ greedy_kernel(VerifyArgs a, int nvec, int S, DivU64 by_S, DivU64 by_K1, bool one
   if (lane == 0) {
     if (any_bad && a.status) atomicOr(a.status, kDataNonfiniteLogit);
     RowSlot* slots = static_cast<RowSlot*>(a.slots);
-    if (S == 1) slots[row].value = key;
-    else atomicMax(&slots[row].value, key);
-    last = arrive_last(a.seq, b, static_cast<unsigned int>(K1) * static_cast<unsigned int>(S)) ? 1u : 0u;
+    if (SPEC_IN(row, a.ws_units, a.status) && SPEC_IN(b, a.B, a.status)) {
+      if (S == 1) slots[row].value = key;
+      else atomicMax(&slots[row].value, key);
+      last = arrive_last(a.seq, b, static_cast<unsigned int>(K1) * static_cast<unsigned int>(S)) ? 1u : 0u;
+    }
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
   __threadfence();  // every lane reads what the other CTAs published

@@ -135,6 +135,12 @@ __device__ __forceinline__ void issue_chunk(const VerifyArgs& a, long long nvec,
                                            long long off, int len, uint4* stage,
                                            unsigned long long* bar) {
   const uint32_t bytes = static_cast<uint32_t>(len) * 16u;
+  if (!(SPEC_IN(static_cast<long long>(b) * (a.K + 1) + i, static_cast<long long>(a.B) * (a.K + 1),
+                a.status) &&
+        SPEC_IN(off + len - 1, nvec, a.status))) {
+    mbar_arrive(bar);  // (debug builds) nothing copied: the stage keeps stale data
+    return;
+  }
   const uint4* trow = static_cast<const uint4*>(a.target) +
                       (static_cast<size_t>(b) * (a.K + 1) + i) * nvec + off;
   if (i < a.K) {
@@ -154,9 +160,9 @@ constexpr int kThreadsA = kThreads + 32;  // 8 consumer warps + 1 producer warp
 // Consumer warps only (named barrier 1): warp 0 merges the parked partials of
 // each (range, pair) over the 8 warps and stores one Partial at its slot
 // (range + pair).
-__device__ __forceinline__ void flush_partials(Partial* partials, const float4* s_pend,
-                                               const long long* s_slot, int npend, int warp,
-                                               int lane) {
+__device__ __forceinline__ void flush_partials(const VerifyArgs& a, Partial* partials,
+                                               const float4* s_pend, const long long* s_slot,
+                                               int npend, int warp, int lane) {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
   if (warp == 0) {
     for (int j = lane; j < npend; j += 32) {
@@ -168,7 +174,7 @@ __device__ __forceinline__ void flush_partials(Partial* partials, const float4* 
       }
       Partial out;
       out.ms_t = v.x; out.z_t = v.y; out.ms_d = v.z; out.z_d = v.w;
-      partials[s_slot[j]] = out;
+      if (SPEC_IN(s_slot[j], a.ws_units, a.status)) partials[s_slot[j]] = out;
     }
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
@@ -245,7 +251,7 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
       if (lane == 0) s_pend[npend * kWarps + warp] = make_float4(mt, zt, md, zd);
       if (tid == 0) s_slot[npend] = c + p;
       if (++npend == kMaxPending2) {
-        flush_partials(partials, s_pend, s_slot, npend, warp, lane);
+        flush_partials(a, partials, s_pend, s_slot, npend, warp, lane);
         npend = 0;
       }
       ++p;
@@ -304,7 +310,7 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
     if (tid == 0) s_slot[npend] = c + p;
     ++npend;
   }
-  flush_partials(partials, s_pend, s_slot, npend, warp, lane);
+  flush_partials(a, partials, s_pend, s_slot, npend, warp, lane);
   if (!ok && a.status) atomicOr(a.status, kWaitTimeout);
 }
 
@@ -394,7 +400,8 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
         pp[t] = static_cast<long long>(i) * a.B + b;
         f[t] = pt.cta_of(pp[t] * nvec);
         l[t] = pt.cta_of((pp[t] + 1) * nvec - 1);
-        if (f[t] + lane <= l[t]) q[t] = partials[f[t] + lane + pp[t]];
+        if (f[t] + lane <= l[t] && SPEC_IN(f[t] + lane + pp[t], a.ws_units, a.status))
+          q[t] = partials[f[t] + lane + pp[t]];
       }
     }
 #pragma unroll
@@ -406,7 +413,8 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
         warp_merge_scaled(md, zd);
         for (int j0 = f[t] + 32; j0 <= l[t]; j0 += 32) {  // rows over more than 32 ranges
           Partial r = Partial{-INFINITY, 0.f, -INFINITY, 0.f};
-          if (j0 + lane <= l[t]) r = partials[j0 + lane + pp[t]];
+          if (j0 + lane <= l[t] && SPEC_IN(j0 + lane + pp[t], a.ws_units, a.status))
+            r = partials[j0 + lane + pp[t]];
           warp_merge_scaled(r.ms_t, r.z_t);
           warp_merge_scaled(r.ms_d, r.z_d);
           merge_scaled(mt, zt, r.ms_t, r.z_t);
@@ -581,7 +589,8 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
     for (int i = lane; i <= Klast; i += 32) {
       const long long p = static_cast<long long>(i) * a.B + b;
       const int f = pt.cta_of(p * nvec), l = pt.cta_of((p + 1) * nvec - 1);
-      for (int c = f; c <= l; ++c) partials[c + p] = Partial{0.f, 0.f, 0.f, 0.f};
+      for (int c = f; c <= l; ++c)
+        if (SPEC_IN(c + p, a.ws_units, a.status)) partials[c + p] = Partial{0.f, 0.f, 0.f, 0.f};
     }
   }
 
@@ -682,7 +691,7 @@ decide_sample_kernel(VerifyArgs a, StreamPartition pt) {
   }
 
   // ---- outputs (warp 0 of rank 0) ----------------------------------------
-  if (rank == 0 && warp == 0) {
+  if (rank == 0 && warp == 0 && SPEC_IN(b, a.B, a.status) && SPEC_IN(n, K1, a.status)) {
     const int32_t* x = a.tokens + static_cast<size_t>(b) * K;
     int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
     for (int j = lane; j < K1; j += 32)

@@ -264,6 +264,10 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
     if (want_draw && (taken < 2 || vld(sh.draws_finished) >= taken - 1)) {
       __threadfence_block();
       const Job j = sh.jobs[taken % kReq];
+      if (!(SPEC_IN(j.b, g.B, a.status) && SPEC_IN(j.n, K + 1, a.status))) {
+        ok = false;  // (debug builds) a draw outside the batch: stop this CTA
+        break;
+      }
       const int per = j.residual ? kLs : kStageVec;
       const uint4* trow = T + (static_cast<size_t>(j.b) * (K + 1) + j.n) * nvec;
       const uint4* drow = j.residual ? D + (static_cast<size_t>(j.b) * K + j.n) * nvec : nullptr;
@@ -329,6 +333,11 @@ __device__ __forceinline__ void run_producer(const VerifyArgs& a, const FusedGeo
         coff = (jj - K * g.segs) * 2 * kFusedSeg;
         cend = min(coff + 2 * kFusedSeg, nvec);
         cdrow = nullptr;
+      }
+      if (!(SPEC_IN(cb, g.B, a.status) && SPEC_IN(i, K + 1, a.status) &&
+            SPEC_IN(cend - 1, nvec, a.status))) {
+        ok = false;  // (debug builds) a unit outside the batch: stop this CTA
+        break;
       }
       ctrow = T + (static_cast<size_t>(cb) * (K + 1) + i) * nvec;
       cnext = coff;
@@ -565,8 +574,10 @@ __device__ __forceinline__ void run_arrivals(const VerifyArgs& a, const FusedGeo
       mbar_arrive(&sh.part_free[uu % kPartBuf]);
       const int b = sh.ub[uu % kUQ];
       const long long tau = sh.utau[uu % kUQ];
-      partials[tau] = mine;
-      red_add_release_gpu(&a.seq[b].arrivals, 1u);  // the Partial is published first
+      if (SPEC_IN(tau, a.ws_units, a.status) && SPEC_IN(b, g.B, a.status)) {
+        partials[tau] = mine;
+        red_add_release_gpu(&a.seq[b].arrivals, 1u);  // the Partial is published first
+      }
     }
     u += nb;
     if (lane == 0) vst(sh.units_folded, u);
@@ -591,6 +602,7 @@ __device__ __noinline__ Job decide(const VerifyArgs& a, const FusedGeom& g, int 
   const float s = a.scale;
   const float* u = a.uniforms + static_cast<size_t>(b) * K1;
   Partial* parts = static_cast<Partial*>(a.partials) + static_cast<size_t>(b) * g.tps;
+  if (!SPEC_IN(static_cast<long long>(b + 1) * g.tps - 1, a.ws_units, a.status)) parts = nullptr;
   float MSt[kRounds], Zt[kRounds], MSd[kRounds], Zd[kRounds], gx[kRounds], gy[kRounds], ui[kRounds];
   int xr[kRounds];
   // one lane's acquire saw every unit's partial; order every lane's loads
@@ -623,7 +635,8 @@ __device__ __noinline__ Job decide(const VerifyArgs& a, const FusedGeom& g, int 
   for (int w0 = 0; w0 < g.tps; w0 += kScratch) {
     const int cnt = min(kScratch, g.tps - w0);
     for (int j = lane; j < cnt; j += 32) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + w0 + j));
+      const float4 v = parts ? __ldcg(reinterpret_cast<const float4*>(parts + w0 + j))
+                             : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
       scratch[j] = Partial{v.x, v.y, v.z, v.w};
     }
     __syncwarp();
@@ -643,7 +656,7 @@ __device__ __noinline__ Job decide(const VerifyArgs& a, const FusedGeom& g, int 
     }
     __syncwarp();
   }
-  for (int j = lane; j < g.tps; j += 32)
+  for (int j = lane; parts && j < g.tps; j += 32)
     reinterpret_cast<float4*>(parts)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 
   int n = K, bad = 0;
@@ -661,8 +674,10 @@ __device__ __noinline__ Job decide(const VerifyArgs& a, const FusedGeom& g, int 
         if (!(isfinite(MSd[r]) && isfinite(Zd[r]) && Zd[r] > 0.f)) bad |= kDataNonfiniteLogit;
         const float px = ex2(fmaf(gx[r], s, -MSt[r])) / Zt[r];
         const float qx = ex2(fmaf(gy[r], s, -MSd[r])) / Zd[r];
-        if (a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
-        if (a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
+        if (SPEC_IN(static_cast<long long>(b) * K + i, static_cast<long long>(a.B) * K, a.status)) {
+          if (a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
+          if (a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
+        }
         rej = !(ui[r] * qx < px);
         nr = qx > 0.f && fabsf(ui[r] - fminf(1.f, px / qx)) < kBandF;
       }
@@ -778,6 +793,7 @@ __device__ __noinline__ bool finish_draw(const VerifyArgs& a, const FusedGeom& g
     token = __shfl_sync(0xffffffffu, tok, lstar);
     near = __shfl_sync(0xffffffffu, nr, lstar);
   }
+  if (!SPEC_IN(b, g.B, a.status) || !SPEC_IN(n, K1, a.status)) return false;
   const int32_t* x = a.tokens + static_cast<size_t>(b) * K;
   int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
   for (int jj = lane; jj < K1; jj += 32)

@@ -121,8 +121,10 @@ seq_sample_kernel(VerifyArgs a, int nvec) {
           const float gy = staged_elem<E>(rows + static_cast<size_t>(K1 + i) * nvec, xc);
           const float px = ex2(fmaf(gx, s, -nt.x)) / nt.y;
           const float qx = ex2(fmaf(gy, s, -nd.x)) / nd.y;
-          if (a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
-          if (a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
+          if (SPEC_IN(static_cast<long long>(b) * K + i, static_cast<long long>(a.B) * K, a.status)) {
+            if (a.p_at) a.p_at[static_cast<size_t>(b) * K + i] = px;
+            if (a.q_at) a.q_at[static_cast<size_t>(b) * K + i] = qx;
+          }
           rej = !(s_u[i] * qx < px);
           nr = qx > 0.f && fabsf(s_u[i] - fminf(1.f, px / qx)) < kBandF;
         }
@@ -242,7 +244,7 @@ seq_sample_kernel(VerifyArgs a, int nvec) {
   }
 
   // ---- outputs (warp 0) ------------------------------------------------
-  if (warp == 0) {
+  if (warp == 0 && SPEC_IN(b, a.B, a.status) && SPEC_IN(n, K1, a.status)) {
     const int token = s_tok;
     for (int j = lane; j < K1; j += 32) {
       int o = -1;

@@ -83,6 +83,10 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
  * Never expected in normal use. */
 #define SPEC_DEVICE_WAIT_TIMEOUT 8
 #define SPEC_DATA_NONFINITE_SCORE 16 /* spec_rejection_cut: a NaN or infinite score */
+/* Debug builds of the library only (compiled with -DSPEC_DEBUG, a test
+ * variant): an index check on a global access failed and the access was
+ * skipped instead of faulting.  A release build never sets it. */
+#define SPEC_DEBUG_BOUNDS 32
 
 /* Per-sequence boundary flags (sampling mode; written when `flags` is given).
  * They mark decisions the kernel took within 1e-6 of a threshold, where a

@@ -242,3 +242,21 @@ def test_c_program_uses_the_boundary_without_python(binding, tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, (run.returncode, run.stderr)
     assert "all checks passed" in run.stdout
+
+
+def test_debug_variant_builds_with_the_same_exports(binding):
+    """The -DSPEC_DEBUG test variant (index checks that report instead of
+    faulting) builds from the same sources and exports the same entry points;
+    the optional NVTX ranges (-DSPEC_NVTX) compile."""
+    import subprocess
+    from draft_verify_acceptance_gb300 import build
+    lib = build.build(debug=True)
+    assert lib.endswith("libspecverify_debug.so")
+    dbg = ctypes.CDLL(lib)
+    for n in binding.EXPORTS:
+        assert hasattr(dbg, n), n
+    src = os.path.join(build.CSRC, "spec_verify.cu")
+    r = subprocess.run([build._nvcc(), "-std=c++17", *build.ARCH, "-DSPEC_NVTX", "-c", src,
+                        "-o", os.devnull, "-I", os.path.join(build.ROOT, "include")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
