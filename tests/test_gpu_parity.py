@@ -419,6 +419,12 @@ DRAFT_SAMPLE_CASES = [
     ("ds_bf16_32000", (8, 4), 32000, torch.bfloat16, 1.0),
     ("ds_bf16_128256", (40,), 128256, torch.bfloat16, 0.7),
     ("ds_f32_152064", (16,), 152064, torch.float32, 0.8),
+    # the persistent row streamer (rows of at most 4096 16-byte vectors):
+    # more rows than SMs, both slot-limit widths, a cold temperature
+    ("ds_bf16_32000_many", (4, 100), 32000, torch.bfloat16, 1.0),
+    ("ds_bf16_32768_limit", (310,), 32768, torch.bfloat16, 0.7),
+    ("ds_f32_16384_limit", (161,), 16384, torch.float32, 1.3),
+    ("ds_bf16_4096_T0.05", (700,), 4096, torch.bfloat16, 0.05),
 ]
 
 
