@@ -133,7 +133,8 @@ struct PairCursor {
 
 __device__ __forceinline__ void issue_chunk(const VerifyArgs& a, long long nvec, int i, int b,
                                            long long off, int len, uint4* stage,
-                                           unsigned long long* bar) {
+                                           unsigned long long* bar, unsigned long long pol_keep,
+                                           unsigned long long pol_drop) {
   const uint32_t bytes = static_cast<uint32_t>(len) * 16u;
   if (!(SPEC_IN(static_cast<long long>(b) * (a.K + 1) + i, static_cast<long long>(a.B) * (a.K + 1),
                 a.status) &&
@@ -143,15 +144,21 @@ __device__ __forceinline__ void issue_chunk(const VerifyArgs& a, long long nvec,
   }
   const uint4* trow = static_cast<const uint4*>(a.target) +
                       (static_cast<size_t>(b) * (a.K + 1) + i) * nvec + off;
+  // the row pairs of draft position 0 -- the likeliest first rejection --
+  // are kept in L2 in preference to the others (streamed evict-first), so
+  // that the decide-and-draw kernel's re-read of the drawn pair more often
+  // finds them there.  Measured: position 0 alone beats positions 0-1 and
+  // position 0 plus the bonus rows (more than L2 keeps under the stream)
+  const unsigned long long pol = i < 1 ? pol_keep : pol_drop;
   if (i < a.K) {
     const uint4* drow = static_cast<const uint4*>(a.draft) +
                         (static_cast<size_t>(b) * a.K + i) * nvec + off;
     mbar_arrive_expect_tx(bar, 2u * bytes);
-    bulk_load(stage, trow, bytes, bar);
-    bulk_load(stage + kChunk2, drow, bytes, bar);
+    bulk_load_hint(stage, trow, bytes, bar, pol);
+    bulk_load_hint(stage + kChunk2, drow, bytes, bar, pol);
   } else {
     mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(stage, trow, bytes, bar);
+    bulk_load_hint(stage, trow, bytes, bar, pol);
   }
 }
 
@@ -215,6 +222,8 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
   // ---- producer warp: one thread keeps kStages2 chunks in flight ---------
   if (warp == kWarps) {
     if (lane == 0) {
+      const unsigned long long pol_keep = make_policy_evict_last();
+      const unsigned long long pol_drop = make_policy_evict_first();
       PairCursor prod(vlo, vhi, pt, a.B);
       bool ok = true;
       long long st, off;
@@ -223,7 +232,8 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
         const int q = k % kStages2;
         if (k >= kStages2 && !mbar_wait_sleep(&empty[q], static_cast<uint32_t>((k / kStages2 - 1) & 1)))
           ok = false;
-        issue_chunk(a, nvec, pi, pb, off, len, ring2 + static_cast<size_t>(q) * 2 * kChunk2, &full[q]);
+        issue_chunk(a, nvec, pi, pb, off, len, ring2 + static_cast<size_t>(q) * 2 * kChunk2, &full[q],
+                    pol_keep, pol_drop);
       }
       if (!ok && a.status) atomicOr(a.status, kWaitTimeout);
     }
