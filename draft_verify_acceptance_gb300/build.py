@@ -56,6 +56,10 @@ def build(force: bool = False, verbose: bool = False, debug: bool = False) -> st
     if not force and not _stale(lib):
         return lib
     os.makedirs(bdir, exist_ok=True)
+    wanted = {src.replace(".cu", ".o") for src in SOURCES}
+    for f in os.listdir(bdir):  # objects of sources no longer in the library
+        if f.endswith(".o") and f not in wanted:
+            os.remove(os.path.join(bdir, f))
     nvcc = _nvcc()
     common = [nvcc, "-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xptxas", "-v",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
