@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table and the CPU baseline")
     ap.add_argument("--line", default=None,
-                    help="time one contrastive-verify or rejection-cut workload alone "
+                    help="time one contrastive-verify, rejection-cut or <workload>+draft_sample line alone "
                          "(--steps launches) and print its line")
     return ap.parse_args()
 
@@ -812,6 +812,9 @@ def run_line(args):
     elif args.line in W.REJECTION_WORKLOADS:
         res = rejection_cut_line(binding, args.line, W.REJECTION_WORKLOADS[args.line], args.steps,
                                  dev, l2, peak)
+    elif args.line.endswith("+draft_sample") and args.line[:-len("+draft_sample")] in W.WORKLOADS:
+        inp = W.workload(args.line[:-len("+draft_sample")])
+        res = draft_sample_line(binding, inp, args.steps, dev, l2, peak)
     else:
         raise SystemExit(f"unknown line {args.line!r}")
     print(json.dumps({"line": args.line, **res}))

@@ -227,8 +227,13 @@ SPEC_API spec_status_t spec_verify_static(const void* target_logits, const void*
  * samples x_i from its distribution q_i).  For each of R rows:
  *
  *   q = softmax(row / T);  x = the smallest token j with C_j > u * S, C the
- *   inclusive running sum of q in token order and S its total (the same
- *   inverse CDF, on the same fixed-point scheme, as spec_verify's draws).
+ *   inclusive running sum of q in token order and S its total (the inverse
+ *   CDF of spec_verify's draws).  C is summed exactly in fixed point: each
+ *   16-byte vector's terms 2^((x - max)/T * log2 e) are rounded once to a
+ *   multiple of 2^-40 (rows that fit a cluster's shared memory) or, for
+ *   longer rows, drawn as spec_verify's bonus draw with K = 0; the two
+ *   roundings can pick different tokens only when u * S lies within about
+ *   1e-7 * S of a step of C.
  *
  *   logits     [R, V]  dtype, device (for example the draft's [B, K, V]
  *              logits, R = B*K).  Rows must be 16-byte aligned: V times the

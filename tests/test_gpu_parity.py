@@ -414,17 +414,21 @@ def test_bad_arguments_raise_before_launch(lib):
 
 
 DRAFT_SAMPLE_CASES = [
-    # (name, rows shape, V, dtype, T): fused-kernel rows, two-kernel rows
+    # (name, rows shape, V, dtype, T): clusters of 1, 2, 4 and 8 CTAs per
+    # row, short and ragged warp ranges, more rows than resident CTAs, a cold
+    # temperature, and rows too long for a cluster (the K = 0 verify)
     ("ds_f32_short", (5, 3), 1000, torch.float32, 1.0),
+    ("ds_f32_tiny", (7,), 36, torch.float32, 1.0),
     ("ds_bf16_32000", (8, 4), 32000, torch.bfloat16, 1.0),
+    ("ds_bf16_65536_c2", (12,), 65536, torch.bfloat16, 0.9),
     ("ds_bf16_128256", (40,), 128256, torch.bfloat16, 0.7),
     ("ds_f32_152064", (16,), 152064, torch.float32, 0.8),
-    # the persistent row streamer (rows of at most 4096 16-byte vectors):
-    # more rows than SMs, both slot-limit widths, a cold temperature
-    ("ds_bf16_32000_many", (4, 100), 32000, torch.bfloat16, 1.0),
+    ("ds_bf16_32000_many", (4, 300), 32000, torch.bfloat16, 1.0),
     ("ds_bf16_32768_limit", (310,), 32768, torch.bfloat16, 0.7),
     ("ds_f32_16384_limit", (161,), 16384, torch.float32, 1.3),
     ("ds_bf16_4096_T0.05", (700,), 4096, torch.bfloat16, 0.05),
+    ("ds_bf16_393216_c8", (3,), 393216, torch.bfloat16, 1.0),
+    ("ds_bf16_400000_verify", (3,), 400000, torch.bfloat16, 1.0),
 ]
 
 
@@ -448,6 +452,26 @@ def test_draft_sample_parity(lib, name, shape, V, dtype, T):
     tol = 1e-5 if dtype == torch.float32 else 2e-3
     assert np.abs(q - ref["q_at"]).max() <= tol, name
     assert int(ws.count_nonzero().item()) == 0  # left zero-filled
+
+
+def test_draft_sample_nonfinite_rows(lib):
+    """A row with a NaN, one with +inf and one with no finite logit set
+    SPEC_DATA_NONFINITE_LOGIT; the finite rows still equal the oracle."""
+    g = torch.Generator().manual_seed(77)
+    for V, dtype in ((32000, torch.bfloat16), (152064, torch.float32)):
+        x = (torch.randn(6, V, generator=g) * 3.0).to(dtype)
+        x[1, 17] = float("nan")
+        x[2, V - 3] = float("inf")
+        x[3, :] = float("-inf")
+        u = torch.rand(6, generator=g)
+        tok, q, status = lib.draft_sample(_dev(x), _dev(u), 1.0, debug=True)
+        torch.cuda.synchronize()
+        assert int(status.item()) & lib.DATA_NONFINITE_LOGIT
+        fine = [0, 4, 5]
+        ref = oracle.draft_sample_ref(W.as_numpy_logits(x[fine]), u[fine].numpy(), 1.0)
+        ok = ref["flags"] == 0
+        np.testing.assert_array_equal(tok.cpu().numpy()[fine][ok], ref["tokens"][ok])
+        assert ((tok.cpu().numpy() >= 0) & (tok.cpu().numpy() < V)).all()
 
 
 def test_draft_sample_rejects_unaligned_rows(lib):
