@@ -178,6 +178,8 @@ KERNEL_SOURCES = {
                           "launch.h"],
     "cut_warp_kernel": ["rejection_cut.cu", "launch.h"],
     "scd_row_kernel": ["verify_scd.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
+    "row_sample_kernel": ["verify_draft_sample.cu", "sample_common.cuh", "device_common.cuh",
+                          "launch.h"],
 }
 
 
@@ -688,8 +690,16 @@ def draft_sample_line(binding, inp, steps, dev, l2, peak):
     sec = GraphTimer(launch, steps, 3, stream, dev).per_launch()
     del launch, copies
     torch.cuda.empty_cache()
+    achieved = nbytes / sec / 1e9
+    row_bytes = inp.V * s
+    kernel = "row_sample_kernel" if row_bytes % 16 == 0 and row_bytes <= 8 * 96 * 1024 else None
     return {"us_per_step": sec * 1e6, "rows_per_s": inp.B * inp.K / sec, "bytes": nbytes,
-            "GB_per_s": nbytes / sec / 1e9, "frac_hbm": nbytes / sec / 1e9 / peak}
+            "GB_per_s": achieved, "frac_hbm": achieved / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "algorithmic_bytes_per_launch": nbytes,
+                         "kernel": kernel,
+                         "traffic": committed_traffic(inp.name + "+draft_sample", kernel)
+                         if kernel else None}}
 
 
 def early_exit_line(binding, inp, steps, dev, l2, peak, parallel_sec):

@@ -350,6 +350,10 @@ scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, doubl
         look = ci < ncs && s_ck[ci][tid] == k && s_cm[ci][tid] >= thr;
       }
       unsigned long long w = 0;
+      if (!__any_sync(0xffffffffu, look)) {  // no head vector in this warp's tile
+        if (lane == 0) tws[k * kWarpsS + warp] = 0ull;
+        continue;
+      }
       if (look) {
         const uint4 wt = __ldg(trow + v);
         if (vec_max<E>(wt) >= thr) {
