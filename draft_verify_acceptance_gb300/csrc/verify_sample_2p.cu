@@ -163,6 +163,42 @@ __device__ __forceinline__ void issue_chunk(const VerifyArgs& a, long long nvec,
 }
 
 constexpr int kThreadsA = kThreads + 32;  // 8 consumer warps + 1 producer warp
+constexpr int kHalfA = kThreads / 2;      // consumer threads per row of a stage
+
+// Fold up to four 16-byte vectors of one row into a row accumulator (the
+// same steps as acc_vectors_impl on two): one offset update and rescale per
+// 4 * VEC logits.  kFull: all four are valid.
+template <typename E, bool kFull>
+__device__ __forceinline__ void acc4(RowAcc& A, const uint4 (&w)[4], int nvalid, float s) {
+  constexpr int VEC = Staged<E>::kVec;
+  constexpr int NP = 2 * VEC;  // pairs in four vectors
+  typename Staged<E>::Max pm = Staged<E>::max_init();
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (kFull || j < nvalid) Staged<E>::max_update(pm, w[j]);
+  const float nm = fmaxf(A.ms, Staged<E>::max_value(pm) * s);
+  const float f = (A.ms == nm) ? 1.f : ex2(A.ms - nm);
+  const float2 s2 = make_float2(s, s), nm2 = make_float2(-nm, -nm);
+  float2 e[NP];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float2 x[VEC / 2];
+    unpack_pairs<E>(w[j], x);
+#pragma unroll
+    for (int k = 0; k < VEC / 2; ++k) {
+      const float2 t = ffma2(x[k], s2, nm2);
+      e[j * (VEC / 2) + k] = (kFull || j < nvalid) ? make_float2(ex2(t.x), ex2(t.y))
+                                                   : make_float2(0.f, 0.f);
+    }
+  }
+#pragma unroll
+  for (int h = NP / 2; h > 0; h >>= 1)
+#pragma unroll
+    for (int k = 0; k < h; ++k) e[k] = fadd2(e[k], e[k + h]);
+  const float zn = fmaf(A.z, f, e[0].x + e[0].y);
+  A.z = (nm == -INFINITY) ? 0.f : zn;
+  A.ms = nm;
+}
 
 // Consumer warps only (named barrier 1): warp 0 merges the parked partials of
 // each (range, pair) over the 8 warps and stores one Partial at its slot
@@ -186,7 +222,7 @@ __device__ __forceinline__ void flush_partials(const VerifyArgs& a, Partial* par
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
-static_assert(kChunk2 == 2 * kThreads, "two vectors per consumer thread per row and stage");
+static_assert(kChunk2 == 4 * kHalfA, "four vectors per consumer thread of a row per stage");
 
 template <typename E>
 __global__ void __launch_bounds__(kThreadsA)
@@ -241,38 +277,45 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
   }
 
   // ---- consumer warps -----------------------------------------------------
+  // Warps 0-3 fold the stage's target vectors, warps 4-7 its draft vectors
+  // (for a bonus row: the first and the second half of the double-length
+  // target chunk), four vectors a thread, into one accumulator per thread.
   // Per-pair facts are set once per pair; per chunk only 32-bit arithmetic.
   Partial* partials = static_cast<Partial*>(a.partials);
+  const int grp = warp >> 2, gtid = tid & (kHalfA - 1);  // row group, thread in group
   long long pos = vlo;
   long long p = static_cast<long long>(pt.by_nvec(vlo));  // current pair
   long long pair_end = (p + 1) * nvec;                     // its end in the flat space
-  int in_pair = static_cast<int>(vlo - p * nvec);          // vectors of the pair before pos
   int ci = static_cast<int>(pt.by_B(p));                   // (position, sequence) of pair p
   int cb = static_cast<int>(p - static_cast<long long>(ci) * a.B);
   int npend = 0;
-  RowAcc At{-INFINITY, 0.f}, Ad{-INFINITY, 0.f};
+  RowAcc A{-INFINITY, 0.f};
   bool ok = true;
+  // this warp's parked normaliser: the draft row's for group 1 of a draft pair
+  auto park = [&](bool draft_pair) {
+    float m = A.ms, z = A.z;
+    warp_merge_scaled(m, z);
+    if (lane == 0)
+      s_pend[npend * kWarps + warp] = (grp == 1 && draft_pair) ? make_float4(-INFINITY, 0.f, m, z)
+                                                               : make_float4(m, z, -INFINITY, 0.f);
+    if (tid == 0) s_slot[npend] = c + p;
+    ++npend;
+  };
 
   for (int k = 0; pos < vhi; ++k) {
     if (pos == pair_end) {  // pair change: park the finished pair's partial
-      float mt = At.ms, zt = At.z, md = Ad.ms, zd = Ad.z;
-      warp_merge_scaled(mt, zt);
-      warp_merge_scaled(md, zd);
-      if (lane == 0) s_pend[npend * kWarps + warp] = make_float4(mt, zt, md, zd);
-      if (tid == 0) s_slot[npend] = c + p;
-      if (++npend == kMaxPending2) {
+      park(ci < a.K);
+      if (npend == kMaxPending2) {
         flush_partials(a, partials, s_pend, s_slot, npend, warp, lane);
         npend = 0;
       }
       ++p;
       pair_end += nvec;
-      in_pair = 0;
       if (++cb == a.B) {
         cb = 0;
         ++ci;
       }
-      At = RowAcc{-INFINITY, 0.f};
-      Ad = RowAcc{-INFINITY, 0.f};
+      A = RowAcc{-INFINITY, 0.f};
     }
     const bool has_draft = ci < a.K;  // a (target, draft) pair, else a bonus row
     long long end = pos + (has_draft ? kChunk2 : 2 * kChunk2);
@@ -281,45 +324,33 @@ norm_stream_kernel(VerifyArgs a, StreamPartition pt) {
     const int len = static_cast<int>(end - pos);
     const int q = k % kStages2;
     if (!mbar_wait_sleep(&full[q], static_cast<uint32_t>((k / kStages2) & 1))) ok = false;
-    const uint4* stage_t = ring2 + static_cast<size_t>(q) * 2 * kChunk2;
-    const uint4* stage_d = stage_t + kChunk2;
-    // draft pair: wt = target vectors, wd = draft vectors of the same range;
-    // bonus row: wt and wd are the two halves of a double-length target chunk
+    // draft pair: group 0 reads the target half of the stage, group 1 the
+    // draft half, len vectors each; bonus row: the two halves of the chunk
+    const uint4* src = ring2 + static_cast<size_t>(q) * 2 * kChunk2 + grp * kChunk2;
     const int half = has_draft ? len : (len < kChunk2 ? len : kChunk2);
-    const int rest = has_draft ? len : len - half;
-    const int nvalid = (tid < half ? 1 : 0) + (tid + kThreads < half ? 1 : 0);
-    const int nvalid2 = (tid < rest ? 1 : 0) + (tid + kThreads < rest ? 1 : 0);
-    uint4 wt[2], wd[2];
-    if (rest == kChunk2) {  // a full stage (block-uniform): no per-element selects
-      wt[0] = stage_t[tid];
-      wt[1] = stage_t[tid + kThreads];
-      wd[0] = stage_d[tid];
-      wd[1] = stage_d[tid + kThreads];
+    const int cnt = grp == 0 ? half : (has_draft ? len : len - half);
+    uint4 w[4];
+    if (cnt == kChunk2) {  // a full half-stage (warp-uniform): no per-element selects
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = src[gtid + j * kHalfA];
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[q]);  // this warp is done reading stage q
-      acc_vectors_full<E>(At, wt, s);
-      acc_vectors_full<E>(has_draft ? Ad : At, wd, s);
+      acc4<E, true>(A, w, 4, s);
     } else {
-      if (nvalid > 0) wt[0] = stage_t[tid];
-      if (nvalid > 1) wt[1] = stage_t[tid + kThreads];
-      if (nvalid2 > 0) wd[0] = stage_d[tid];
-      if (nvalid2 > 1) wd[1] = stage_d[tid + kThreads];
+      int nvalid = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (gtid + j * kHalfA < cnt) {
+          w[j] = src[gtid + j * kHalfA];
+          nvalid = j + 1;
+        }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[q]);
-      acc_vectors<E>(At, wt, nvalid, s);
-      acc_vectors<E>(has_draft ? Ad : At, wd, nvalid2, s);
+      acc4<E, false>(A, w, nvalid, s);
     }
     pos = end;
-    in_pair += len;
   }
-  {  // the last pair
-    float mt = At.ms, zt = At.z, md = Ad.ms, zd = Ad.z;
-    warp_merge_scaled(mt, zt);
-    warp_merge_scaled(md, zd);
-    if (lane == 0) s_pend[npend * kWarps + warp] = make_float4(mt, zt, md, zd);
-    if (tid == 0) s_slot[npend] = c + p;
-    ++npend;
-  }
+  park(ci < a.K);  // the last pair
   flush_partials(a, partials, s_pend, s_slot, npend, warp, lane);
   if (!ok && a.status) atomicOr(a.status, kWaitTimeout);
 }
