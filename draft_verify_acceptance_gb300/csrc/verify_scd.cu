@@ -121,7 +121,7 @@ __device__ __forceinline__ float contrast(float t, float a, float thr) {
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kThreadsS, 4)
+__global__ void __launch_bounds__(kThreadsS, 5)
 scd_row_kernel(VerifyArgs a, const void* amateur, long long nvec, float s, double L, float Lmag) {
   constexpr int VEC = Staged<E>::kVec;
   cg::cluster_group cluster = cg::this_cluster();
