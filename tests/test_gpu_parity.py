@@ -428,6 +428,8 @@ DRAFT_SAMPLE_CASES = [
     ("ds_f32_16384_limit", (161,), 16384, torch.float32, 1.3),
     ("ds_bf16_4096_T0.05", (700,), 4096, torch.bfloat16, 0.05),
     ("ds_bf16_393216_c8", (3,), 393216, torch.bfloat16, 1.0),
+    ("ds_bf16_100008_c4_ragged", (6,), 100008, torch.bfloat16, 1.1),
+    ("ds_f32_24580_c2_ragged", (9,), 24580, torch.float32, 0.9),
     ("ds_bf16_400000_verify", (3,), 400000, torch.bfloat16, 1.0),
 ]
 
