@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["spec_verify.cu", "verify_greedy.cu", "verify_sample.cu", "verify_sample_fused.cu", "verify_sample_seq.cu", "verify_sample_2p.cu", "verify_draft_sample.cu", "verify_scd.cu", "rejection_cut.cu",
+SOURCES = ["spec_verify.cu", "verify_greedy.cu", "verify_sample.cu", "verify_sample_fused.cu", "verify_sample_seq.cu", "verify_sample_ee.cu", "verify_sample_2p.cu", "verify_draft_sample.cu", "verify_scd.cu", "rejection_cut.cu",
            "spec_verify_static.cu"]
 
 

@@ -35,6 +35,7 @@ cudaError_t device_info(int device, DeviceInfo* out) {
     if (e == cudaSuccess) e = seq_sample_prepare();
     if (e == cudaSuccess) e = sample_2p_prepare(&d);
     if (e == cudaSuccess) e = row_sample_prepare();
+    if (e == cudaSuccess) e = sample_ee_prepare();
     if (e == cudaSuccess) e = scd_prepare();
     g_info[device] = d;
     g_err[device] = e;

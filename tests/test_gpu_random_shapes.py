@@ -74,7 +74,9 @@ def test_random_shape_parity(lib, case):
         assert (out[b, nb + 1:] == -1).all()
     if mode != "greedy" and K > 0:
         tol = 1e-5 if dtype == torch.float32 else 2e-3
-        # early exit without a second phase reports position 0 only
-        cols = slice(0, 1) if (mode == "sample_early_exit" and (n == 0).all()) else slice(None)
-        assert np.abs(res["p_at"].cpu().numpy()[:, cols] - ref["p_at"][:, cols]).max() <= tol, label
-        assert np.abs(res["q_at"].cpu().numpy()[:, cols] - ref["q_at"][:, cols]).max() <= tol, label
+        # early exit reports at least the positions whose rows it read: 0..n
+        read = np.ones((B, K), bool)
+        if mode == "sample_early_exit":
+            read = np.arange(K)[None, :] <= ref["accepted_len"][:, None]
+        assert np.abs(res["p_at"].cpu().numpy() - ref["p_at"])[read].max() <= tol, label
+        assert np.abs(res["q_at"].cpu().numpy() - ref["q_at"])[read].max() <= tol, label
