@@ -102,14 +102,6 @@ cudaError_t launch_sample_2p(const VerifyArgs& a, const DeviceInfo& dev, int C,
 cudaError_t launch_sample_early_exit(const VerifyArgs& a, const DeviceInfo& dev, int C,
                                      cudaStream_t stream);
 
-// Early exit for batches of at most one cluster per SM: one cluster of C CTAs
-// per sequence walks the positions in order, each row pair staged in shared
-// memory, and draws at the first rejection.
-int ee_cluster(long long nvec);
-bool ee_fits(const VerifyArgs& a, int C);
-cudaError_t sample_ee_prepare();
-cudaError_t launch_sample_ee(const VerifyArgs& a, int C, cudaStream_t stream);
-
 // The drafter's sampling step: one cluster of C CTAs per row, the row staged
 // in shared memory (rows of up to 8 * 96 KiB).
 int row_sample_cluster(long long nvec);

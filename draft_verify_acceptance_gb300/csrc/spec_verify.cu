@@ -9,6 +9,7 @@
 #include "../../include/spec_verify.h"
 #include "device_common.cuh"
 #include "launch.h"
+#include "launch_ee.h"
 
 
 namespace specv {

@@ -39,6 +39,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "launch_ee.h"
 #include "sample_common.cuh"
 
 namespace cg = cooperative_groups;
