@@ -346,6 +346,33 @@ def test_data_errors_set_status_and_stay_in_range(lib, what):
     np.testing.assert_array_equal(g["out_tokens"][ok], ref["out_tokens"][ok])
 
 
+@pytest.mark.parametrize("what", ["token", "nan", "posinf", "uniform", "neginf_row"])
+def test_early_exit_cluster_data_errors(lib, what):
+    """Data errors at position 0 (whose rows every schedule reads) on the
+    early-exit kernel whose clusters walk the positions: the same status as
+    the oracle, outputs in range, the other sequences unaffected."""
+    inp = W.make_inputs(6, 3, 40000, dtype=torch.float32, seed=13, name=what, target_std=3.0,
+                        independent_draft=True)
+    if what == "token":
+        inp.tokens[2, 0] = 40000
+    elif what == "nan":
+        inp.target[3, 0, 17] = float("nan")
+    elif what == "posinf":
+        inp.draft[1, 0, 5] = float("inf")
+    elif what == "uniform":
+        inp.uniforms[4, 0] = 1.0
+    else:
+        inp.target[0, 0, :] = float("-inf")
+    g, ref = run_gpu_mode(lib, inp, "sample_early_exit"), run_oracle(inp)
+    assert int(g["status"][0]) == ref["status"] != 0, what
+    assert ((g["accepted_len"] >= 0) & (g["accepted_len"] <= 3)).all()
+    assert ((g["out_tokens"] >= -1) & (g["out_tokens"] < 40000)).all()
+    good = ref["accepted_len"] >= 0
+    ok = good & (ref["flags"] == 0)
+    np.testing.assert_array_equal(g["accepted_len"][ok], ref["accepted_len"][ok])
+    np.testing.assert_array_equal(g["out_tokens"][ok], ref["out_tokens"][ok])
+
+
 def test_greedy_data_errors(lib):
     inp = W.make_inputs(5, 3, 3000, dtype=torch.bfloat16, mode=W.MODE_GREEDY, seed=12)
     inp.target[1, 2, 100] = float("nan")
