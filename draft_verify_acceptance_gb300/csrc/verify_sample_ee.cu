@@ -14,17 +14,17 @@
 // Design: each CTA stages its slice of the position's target row and draft
 // row in shared memory (TMA bulk copies of 16 KiB, one mbarrier each), so a
 // row crosses HBM once and the draw at the rejected position reads nothing
-// again.  Per position: (1) the slices' maxima as the copies land, exchanged
-// over the cluster through DSMEM; (2) the normalisers Z = sum 2^(x*s - M*s)
-// from shared memory, exchanged likewise; (3) every CTA takes the same
-// accept decision from the same values (the token's two logits are read
-// once from global memory).  At the first rejection (or at the bonus row):
-// the fixed-point masses of max(0, p - q) (or of p) per 16-byte vector, the
-// verifier's scheme, summed per lane with a checkpoint every four steps of
-// 32 vectors; slice masses over DSMEM; the CTA holding u_K * S finds the
-// warp range, the checkpoint group, the step, the lane and the element, and
-// hands the token to rank 0, which writes the outputs.  No workspace, no
-// global atomics; every wait is bounded.
+// again.  Per position: (1) both rows' online normalisers as the copies land
+// (max and sum of 2^(x*s - offset)), exchanged over the cluster through DSMEM
+// in one step; (2) every CTA takes the same accept decision from the same
+// values (the token's two logits are read once from global memory).  At the
+// first rejection (or at the bonus row): the fixed-point masses of
+// max(0, p - q) (or of p) per 16-byte vector, the verifier's scheme, summed
+// per lane with a checkpoint every four steps of 32 vectors; slice masses
+// over DSMEM; the CTA holding u_K * S finds the warp range, the checkpoint
+// group, the step, the lane and the element, and writes the outputs.  Two
+// cluster exchanges per draw plus one per accepted position; no workspace,
+// no global atomics; every wait is bounded.
 #include <cooperative_groups.h>
 
 #include <cfloat>
@@ -62,23 +62,6 @@ __host__ __device__ __forceinline__ long long ee_smem(long long nvec, int C) {
   return 2 * nvs * 16 + static_cast<long long>(ee_groups(static_cast<int>(nvs))) * kWarpsE * 32 * 8;
 }
 
-// Sum of the terms 2^(x_k * s - ms) of one vector (element order).
-template <typename E>
-__device__ __forceinline__ float vec_sum(const uint4 w, float s, float ms) {
-  constexpr int VEC = Staged<E>::kVec;
-  float2 x[VEC / 2];
-  unpack_pairs<E>(w, x);
-  const float2 s2 = make_float2(s, s), m2 = make_float2(-ms, -ms);
-  float acc = 0.f;
-#pragma unroll
-  for (int k = 0; k < VEC / 2; ++k) {
-    const float2 t = ffma2(x[k], s2, m2);
-    acc = __fadd_rn(acc, ex2(t.x));
-    acc = __fadd_rn(acc, ex2(t.y));
-  }
-  return acc;
-}
-
 // The fixed-point residual mass of staged vector v (max(0, p - q), or p).
 template <typename E, bool kInt = false>
 __device__ __forceinline__ unsigned long long vec_mass(const uint4* st, const uint4* sd, int v,
@@ -95,24 +78,6 @@ __device__ __forceinline__ unsigned long long vec_mass(const uint4* st, const ui
     for (int q = 0; q < VEC; ++q) xd[q] = -INFINITY;
   }
   return vec_weight_scaled<VEC, kInt>(xt, xd, MSt, invZt, MSd, invZd, s, residual, r);
-}
-
-__device__ __forceinline__ float2 warp_max2(float2 v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, o));
-    v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, o));
-  }
-  return v;
-}
-// Butterfly sums: every lane ends with the same bits.
-__device__ __forceinline__ float2 warp_sum2(float2 v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-  }
-  return v;
 }
 
 template <typename E>
@@ -140,11 +105,11 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
   uint4* sd = smem + nvs;  // [nvs] its draft slice
   unsigned long long* cp = reinterpret_cast<unsigned long long*>(smem + 2 * static_cast<size_t>(nvs));
   __shared__ __align__(8) unsigned long long bar_t[kMaxChunksE], bar_d[kMaxChunksE];
-  __shared__ float2 s_wf[kWarpsE];                 // per-warp (target, draft) maxima, then sums
-  __shared__ float2 s_m[kMaxCE], s_z[kMaxCE];      // pushed by each rank
+  __shared__ float4 s_wn[kWarpsE];                 // per-warp (target, draft) normalisers
+  __shared__ float4 s_n[2][kMaxCE];                // pushed by each rank, per position parity
   __shared__ unsigned long long s_wm[kWarpsE];     // per-warp masses
   __shared__ unsigned long long s_mass[2][kMaxCE]; // pushed by each rank, per round
-  __shared__ int s_tok[2];                         // pushed by the crossing CTA to rank 0
+  __shared__ int s_tok[2];                         // the drawn token and its near flag
   __shared__ int s_dec[3];                         // the position's rejection, near flag, errors
   __shared__ int s_sel[2];                         // crossing warp and group
   __shared__ unsigned long long s_tl;              // threshold left inside the group
@@ -207,8 +172,8 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
       dx = load_one<E>(dbase + static_cast<size_t>(i) * a.V * esz, xc);
     }
 
-    // ---- (1) maxima as the copies land ------------------------------------
-    typename Staged<E>::Max pt = Staged<E>::max_init(), pd = Staged<E>::max_init();
+    // ---- (1) online normalisers as the copies land, one exchange ----------
+    RowAcc At{-INFINITY, 0.f}, Ad{-INFINITY, 0.f};
     bool ok = true;
     for (int c = 0; c < nch; ++c) {
       if (!mbar_wait_sleep(&bar_t[c], par) || (pair && !mbar_wait_sleep(&bar_d[c], par))) {
@@ -217,71 +182,61 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
       }
       const int c0 = c * kChunkE, cend = min(c0 + kChunkE, nv);
       if (cend - c0 == kChunkE) {  // a full chunk: two vectors of each row a thread
-#pragma unroll
-        for (int k = 0; k < kChunkE / kThreadsE; ++k) {
-          Staged<E>::max_update(pt, st[c0 + k * kThreadsE + tid]);
-          if (pair) Staged<E>::max_update(pd, sd[c0 + k * kThreadsE + tid]);
+        static_assert(kChunkE == 2 * kThreadsE, "two vectors of each row a thread");
+        const uint4 wt[2] = {st[c0 + tid], st[c0 + kThreadsE + tid]};
+        acc_vectors_full<E>(At, wt, s);
+        if (pair) {
+          const uint4 wd[2] = {sd[c0 + tid], sd[c0 + kThreadsE + tid]};
+          acc_vectors_full<E>(Ad, wd, s);
         }
       } else {
-        for (int v = c0 + tid; v < cend; v += kThreadsE) {
-          Staged<E>::max_update(pt, st[v]);
-          if (pair) Staged<E>::max_update(pd, sd[v]);
+        const int v = c0 + tid;
+        const int n2 = (v < cend ? 1 : 0) + (v + kThreadsE < cend ? 1 : 0);
+        uint4 wt[2], wd[2];
+        if (n2 > 0) {
+          wt[0] = st[v];
+          if (pair) wd[0] = sd[v];
         }
+        if (n2 > 1) {
+          wt[1] = st[v + kThreadsE];
+          if (pair) wd[1] = sd[v + kThreadsE];
+        }
+        acc_vectors<E>(At, wt, n2, s);
+        if (pair) acc_vectors<E>(Ad, wd, n2, s);
       }
     }
-    const float2 wmx = warp_max2(make_float2(Staged<E>::max_value(pt), Staged<E>::max_value(pd)));
-    if (lane == 0) s_wf[warp] = wmx;
+    warp_merge_scaled(At.ms, At.z);
+    warp_merge_scaled(Ad.ms, Ad.z);
+    if (lane == 0) s_wn[warp] = make_float4(At.ms, At.z, Ad.ms, Ad.z);
     if (__syncthreads_or(!ok) && tid == 0) s_fail = 1;
     if (!waited) {
       cluster_wait();  // every CTA of the cluster has started
       waited = true;
     }
+    float4* s_nb = s_n[i & 1];  // one buffer per position parity: a peer a
+                                // position ahead never overwrites a value in use
     if (warp == 0) {
-      const float2 m = warp_max2(lane < kWarpsE ? s_wf[lane] : make_float2(-INFINITY, -INFINITY));
+      float4 m = lane < kWarpsE ? s_wn[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      warp_merge_scaled(m.x, m.y);
+      warp_merge_scaled(m.z, m.w);
       if (solo) {
-        if (lane == 0) s_m[0] = m;
+        if (lane == 0) s_nb[0] = m;
       } else if (lane < C) {
-        *cluster.map_shared_rank(&s_m[rank], lane) = m;
+        *cluster.map_shared_rank(&s_nb[rank], lane) = m;
       }
     }
     if (solo) __syncthreads();
     else cluster.sync();
-    float Mt = -INFINITY, Md = -INFINITY;
-    for (int r = 0; r < C; ++r) {
-      Mt = fmaxf(Mt, s_m[r].x);
-      Md = fmaxf(Md, s_m[r].y);
-    }
-    MSt = Mt * s;
-    MSd = Md * s;
-
-    // ---- (2) normalisers from shared memory -------------------------------
-    float2 z = make_float2(0.f, 0.f);
-    for (int v = lo + lane; v < hi; v += 32) {
-      z.x = __fadd_rn(z.x, vec_sum<E>(st[v], s, MSt));
-      if (pair) z.y = __fadd_rn(z.y, vec_sum<E>(sd[v], s, MSd));
-    }
-    z = warp_sum2(z);
-    if (lane == 0) s_wf[warp] = z;
-    __syncthreads();
-    if (warp == 0) {
-      float2 t = lane < kWarpsE ? s_wf[lane] : make_float2(0.f, 0.f);
-      t = warp_sum2(t);
-      if (solo) {
-        if (lane == 0) s_z[0] = t;
-      } else if (lane < C) {
-        *cluster.map_shared_rank(&s_z[rank], lane) = t;
-      }
-    }
-    if (solo) __syncthreads();
-    else cluster.sync();
+    MSt = -INFINITY;
     Zt = 0.f;
+    MSd = -INFINITY;
     Zd = 0.f;
     for (int r = 0; r < C; ++r) {  // rank order: the same bits in every CTA
-      Zt += s_z[r].x;
-      Zd += s_z[r].y;
+      merge_scaled(MSt, Zt, s_nb[r].x, s_nb[r].y);
+      merge_scaled(MSd, Zd, s_nb[r].z, s_nb[r].w);
     }
 
-    // ---- (3) the accept test, the same in every CTA -----------------------
+    // ---- (2) the accept test, the same in every CTA -----------------------
     if (tid == 0) {
       int err = 0, rej = 1, nr = 0;
       if (!(isfinite(MSt) && isfinite(Zt) && Zt > 0.f)) err |= kDataNonfiniteLogit;
@@ -425,22 +380,17 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
         const long long t = (v0 + v) * VEC + ks;
         const int tok = static_cast<int>(t < a.V ? t : a.V - 1);
         const int nr = near_step(theta, off + before + c_prev, off + before + c_cur, S) ? 1 : 0;
-        if (solo) {
-          s_tok[0] = tok;
-          s_tok[1] = nr;
-        } else {
-          int* dst = cluster.map_shared_rank(&s_tok[0], 0);
-          dst[0] = tok;
-          dst[1] = nr;
-        }
+        s_tok[0] = tok;
+        s_tok[1] = nr;
       }
     }
+    __syncthreads();
   }
-  if (solo) __syncthreads();
-  else cluster.sync();  // the token has reached rank 0; no DSMEM access after this point
 
-  // ---- outputs (warp 0 of rank 0) ------------------------------------------
-  if (rank == 0 && warp == 0 && SPEC_IN(b, a.B, a.status) && SPEC_IN(n, K1, a.status)) {
+  // ---- outputs (warp 0 of the CTA that drew; rank 0 when nothing was drawn)
+  // No DSMEM access after the mass exchange: the other CTAs may have left.
+  const int writer = S != 0 ? cstar : 0;
+  if (rank == writer && warp == 0 && SPEC_IN(b, a.B, a.status) && SPEC_IN(n, K1, a.status)) {
     const int token = s_tok[0], near = s_tok[1];
     const int32_t* x = a.tokens + static_cast<size_t>(b) * K;
     int32_t* out = a.out_tokens + static_cast<size_t>(b) * K1;
@@ -452,7 +402,7 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
       const int st_bits = bad | (s_fail ? kWaitTimeout : 0);
       if (st_bits && a.status) atomicOr(a.status, st_bits);
     }
-  } else if (tid == 0 && s_fail && a.status) {
+  } else if (rank != writer && tid == 0 && s_fail && a.status) {
     atomicOr(a.status, kWaitTimeout);
   }
 }
