@@ -702,21 +702,55 @@ def draft_sample_line(binding, inp, steps, dev, l2, peak):
                          if kernel else None}}
 
 
+def ee_cluster_size(nvec):
+    """The early-exit kernel's cluster size for rows of nvec 16-byte vectors
+    (src: ee_cluster, verify_sample_ee.cu restated): the smallest C in
+    {1, 2, 4, 8} whose two slices and lane checkpoints fit 200 KiB; 0 if none."""
+    for C in (1, 2, 4, 8):
+        nvs = (nvec + C - 1) // C
+        steps = ((nvs + 15) // 16 + 31) // 32
+        if 2 * nvs * 16 + (steps + 3) // 4 * 16 * 32 * 8 <= 200 * 1024:
+            return C
+    return 0
+
+
+def early_exit_schedule(inp, sm_count=152):
+    """The library's early-exit dispatch restated (src: launch_sample):
+    "small_batch" (one CTA per sequence, every row read), "cluster" (one
+    cluster per sequence walking the positions), or "two_phase"."""
+    nvec = inp.V * inp.target.element_size() // 16
+    if inp.B <= sm_count and (2 * inp.K + 1) * nvec * 16 <= 192 * 1024:
+        return "small_batch"
+    return "cluster" if ee_cluster_size(nvec) > 0 else "two_phase"
+
+
 def early_exit_line(binding, inp, steps, dev, l2, peak, parallel_sec):
-    """The same workload in early-exit mode (position 0 first).  Bytes read:
-    position 0's row pairs, plus every row when some sequence accepted x_0
-    (then the full verify runs too); the outputs equal sampling mode's."""
+    """The same workload in early-exit mode; the outputs equal sampling
+    mode's.  Bytes read, by schedule: the small-batch kernel reads every
+    row; the cluster kernel the row pairs of positions 0..n of each sequence
+    (the bonus row instead of a pair at n = K); the two-phase schedule
+    position 0's row pairs, plus every row when some sequence accepted x_0."""
     import torch
     R, stream, launch, (acc, _) = device_setup(binding, inp, dev, l2,
                                                mode=binding.MODE_SAMPLE_EARLY_EXIT)
     sec = GraphTimer(launch, steps, 5, stream, dev).per_launch()
     s = inp.target.element_size()
-    first = 2 * inp.B * inp.V * s + inp.B * 4 + inp.B * 4 + inp.B * (inp.K + 2) * 4
-    full_ran = bool((acc > 0).any().item())  # the last replayed call's outputs
-    read = first + (inp.algorithmic_bytes() if full_ran else 0)
+    small = inp.B * inp.K * 4 + inp.B * 4 + inp.B * (inp.K + 2) * 4  # tokens, u, outputs
+    n = acc.cpu().long()  # the last replayed call's outputs
+    schedule = early_exit_schedule(inp, torch.cuda.get_device_properties(dev).multi_processor_count)
+    if schedule == "small_batch":
+        read = inp.algorithmic_bytes()
+        full_ran = True
+    elif schedule == "cluster":
+        rows = torch.where(n < inp.K, 2 * (n + 1), 2 * inp.K + 1)
+        read = int(rows.sum().item()) * inp.V * s + small
+        full_ran = False
+    else:
+        full_ran = bool((n > 0).any().item())
+        read = 2 * inp.B * inp.V * s + small + (inp.algorithmic_bytes() if full_ran else 0)
     del launch
     torch.cuda.empty_cache()
-    return {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec,
+    return {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec, "schedule": schedule,
             "bytes_read": read, "GB_per_s": read / sec / 1e9, "frac_hbm": read / sec / 1e9 / peak,
             "full_verify_ran": full_ran, "speedup_vs_sampling_mode": parallel_sec / sec}
 

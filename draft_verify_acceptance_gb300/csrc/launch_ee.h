@@ -8,10 +8,8 @@ namespace specv {
 
 // One cluster of C CTAs per sequence, each row pair staged in shared memory;
 // the draw at the first rejection reads nothing again.  ee_cluster: the
-// cluster size the rows need (0: they do not fit); ee_fits: whether every
-// sequence's cluster can be resident at once.
+// cluster size the rows need (0: they do not fit).
 int ee_cluster(long long nvec);
-bool ee_fits(const VerifyArgs& a, int C);
 cudaError_t sample_ee_prepare();
 cudaError_t launch_sample_ee(const VerifyArgs& a, int C, cudaStream_t stream);
 

@@ -1,7 +1,6 @@
-// verify_sample_ee.cu -- early-exit speculative sampling on sm_103a for
-// batches whose sequences fit one resident wave of clusters: one cluster of
-// C CTAs per sequence walks the draft positions in order and stops reading
-// rows at the first rejection.
+// verify_sample_ee.cu -- early-exit speculative sampling on sm_103a: one
+// cluster of C CTAs per sequence walks the draft positions in order and
+// stops reading rows at the first rejection.
 //
 // Sources (page title, section):
 //   "推测性拒绝采样", 技术原理与步骤 steps 2-4 and 关键保证: x_i is accepted
@@ -29,7 +28,6 @@
 
 #include <cfloat>
 #include <climits>
-#include <mutex>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -425,60 +423,6 @@ cudaError_t sample_ee_prepare() {
     e = cudaFuncSetAttribute(ee_cluster_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
   return e;
-}
-
-// How many clusters of C CTAs of the kernel, with `smem` bytes of dynamic
-// shared memory each, can be resident at once (cached per device and
-// configuration; the occupancy query enqueues no work).
-static int ee_resident_clusters(bool bf16, int C, long long smem) {
-  struct Entry {
-    int dev, C;
-    bool bf16;
-    long long smem;
-    int n;
-  };
-  static std::mutex mu;
-  static Entry cache[16];
-  static int used = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  {
-    std::lock_guard<std::mutex> g(mu);
-    for (int i = 0; i < used; ++i)
-      if (cache[i].dev == dev && cache[i].C == C && cache[i].bf16 == bf16 && cache[i].smem == smem)
-        return cache[i].n;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned int>(C));
-  cfg.blockDim = dim3(kThreadsE);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  const cudaError_t e = bf16 ? cudaOccupancyMaxActiveClusters(&n, ee_cluster_kernel<BF16>, &cfg)
-                             : cudaOccupancyMaxActiveClusters(&n, ee_cluster_kernel<F32>, &cfg);
-  if (e != cudaSuccess) {
-    cudaGetLastError();  // not sticky: clear it
-    return 0;
-  }
-  std::lock_guard<std::mutex> g(mu);
-  cache[used < 16 ? used++ : static_cast<int>((dev + C + smem) & 15)] = Entry{dev, C, bf16, smem, n};
-  return n;
-}
-
-// Whether the early-exit kernel takes this call: rows that fit a cluster of
-// at most 8 CTAs, and every sequence's cluster resident at once (a cluster
-// walks its positions one after another, so a second wave would wait for
-// the first one's whole walk).
-bool ee_fits(const VerifyArgs& a, int C) {
-  if (C < 1 || C > kMaxCE) return false;
-  const long long nvec = static_cast<long long>(a.V) * (a.bf16 ? 2 : 4) / 16;
-  return a.B <= ee_resident_clusters(a.bf16, C, ee_smem(nvec, C));
 }
 
 cudaError_t launch_sample_ee(const VerifyArgs& a, int C, cudaStream_t stream) {

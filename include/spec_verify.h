@@ -145,15 +145,15 @@ SPEC_API size_t spec_verify_workspace_size(int B, int K, int V, int dtype, int m
  * same inverse CDF is taken on p_K.
  * Early-exit sampling mode:  the same outputs as sampling mode, from a
  * schedule that stops reading a sequence's rows at its first rejection.
- * Batches of at most one cluster per SM (B times the cluster size the rows
- * need, at most 8) run one kernel in which each sequence's cluster reads
- * position i's row pair only after positions 0..i-1 were accepted, and draws
- * the replacement from the staged pair.  Larger batches read position 0's
- * row pair of every sequence first, decide position 0 and draw for each
+ * Rows whose target and draft slices fit a cluster of at most 8 CTAs (about
+ * 400 KB per row at most) run one kernel in which each sequence's cluster
+ * reads position i's row pair only after positions 0..i-1 were accepted,
+ * and draws the replacement from the staged pair.  Longer rows read position
+ * 0's row pair of every sequence first, decide position 0 and draw for each
  * sequence that rejects there; only if some sequence accepts x_0 are all rows
  * read and every sequence verified as in sampling mode.  When most sequences
- * reject their first draft token (a poor drafter) this reads 2/(2K+1) of the
- * rows.  16-byte aligned rows with K >= 1 only; other calls run as sampling
+ * reject their first draft token (a poor drafter) this reads about 2/(2K+1)
+ * of the rows.  16-byte aligned rows with K >= 1 only; other calls run as sampling
  * mode.  p_at_draft / q_at_draft (see spec_verify_ex) are written at least
  * for positions 0..n of each sequence (the positions whose rows were read)
  * and device_status covers only the rows read.

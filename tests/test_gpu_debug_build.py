@@ -41,8 +41,10 @@ CASES = [
     ("streaming_bf16_unaligned", 8, 5, 33, torch.bfloat16, "sample", dict(target_std=2.0, draft_noise=1.0)),
     ("early_exit_f32", 6, 3, 20000, torch.float32, "sample_early_exit",
      dict(target_std=5.0, independent_draft=True)),
-    ("early_exit_two_phase_bf16", 200, 3, 32000, torch.bfloat16, "sample_early_exit",
+    ("early_exit_waves_bf16", 200, 3, 32000, torch.bfloat16, "sample_early_exit",
      dict(target_std=3.0, independent_draft=True)),
+    ("early_exit_two_phase_bf16", 3, 2, 400000, torch.bfloat16, "sample_early_exit",
+     dict(target_std=3.0, draft_noise=0.5)),
     ("greedy_one_word", 64, 8, 3000, torch.bfloat16, "greedy", dict(target_std=4.0)),
     ("greedy_segments", 2, 2, 200000, torch.float32, "greedy", dict(target_std=4.0)),
 ]

@@ -209,11 +209,11 @@ def test_greedy_parity(lib, name, B, K, V, dtype, recipe):
 
 
 EARLY_EXIT_CASES = [
-    # (name, B, K, V, dtype, T, recipe).  One cluster per sequence (at most one
-    # per SM): low acceptance, moderate, high (every position walked), K = 1,
-    # clusters of 1, 2 and 4 CTAs.  The two-phase schedule (more clusters than
-    # SMs): low acceptance (phase 2 usually skipped) and moderate (it runs).
-    # Short rows go to the small-batch kernel.
+    # (name, B, K, V, dtype, T, recipe).  One cluster per sequence: low
+    # acceptance, moderate, high (every position walked), K = 1, clusters of
+    # 1, 2 and 4 CTAs, more clusters than fit at once.  The two-phase schedule
+    # (rows too long for a cluster of 8): low acceptance (phase 2 usually
+    # skipped) and moderate (it runs).  Short rows go to the small-batch kernel.
     ("ee_f32_independent", 12, 16, 20000, torch.float32, 0.8, dict(target_std=5.0, independent_draft=True)),
     ("ee_bf16_noise", 48, 5, 40000, torch.bfloat16, 1.0, dict(target_std=4.0, zipf_s=1.1, draft_noise=1.0)),
     ("ee_bf16_close", 16, 4, 32000, torch.bfloat16, 1.0, dict(target_std=3.0, draft_noise=0.3)),
@@ -221,8 +221,10 @@ EARLY_EXIT_CASES = [
     ("ee_bf16_K1", 30, 1, 100000, torch.bfloat16, 0.7, dict(target_std=3.0, draft_noise=1.0)),
     ("ee_bf16_c2", 10, 6, 65536, torch.bfloat16, 0.8, dict(target_std=3.0, draft_noise=0.3)),
     ("ee_bf16_c4", 16, 4, 128256, torch.bfloat16, 1.0, dict(target_std=4.0, zipf_s=1.1, draft_noise=1.0)),
-    ("ee_2p_bf16_many", 200, 4, 32000, torch.bfloat16, 1.0, dict(target_std=3.0, independent_draft=True)),
-    ("ee_2p_bf16_wide", 64, 3, 128256, torch.bfloat16, 1.0, dict(target_std=4.0, zipf_s=1.1, draft_noise=1.0)),
+    ("ee_bf16_many", 200, 4, 32000, torch.bfloat16, 1.0, dict(target_std=3.0, independent_draft=True)),
+    ("ee_bf16_wide", 64, 3, 128256, torch.bfloat16, 1.0, dict(target_std=4.0, zipf_s=1.1, draft_noise=1.0)),
+    ("ee_2p_bf16_long_low", 6, 2, 400000, torch.bfloat16, 1.0, dict(target_std=3.0, independent_draft=True)),
+    ("ee_2p_bf16_long_mid", 6, 3, 400000, torch.bfloat16, 1.0, dict(target_std=3.0, draft_noise=0.5)),
     ("ee_f32_short", 6, 3, 1000, torch.float32, 1.0, dict(target_std=3.0, independent_draft=True)),
 ]
 

@@ -143,3 +143,29 @@ def test_kernel_hash_ignores_comments_only():
     files["verify_greedy.cu"] = "int x = 2; // one\n"
     h2 = bench.kernel_source_hash("greedy_kernel", files.get)
     assert h0 == h1 != h2
+
+
+def test_early_exit_schedule_matches_the_dispatch_rule():
+    """The bench's restatement of the early-exit dispatch: rows whose two
+    slices (and lane checkpoints) fit 200 KiB in a cluster of at most 8 CTAs
+    take the cluster kernel; longer rows the two-phase schedule; small
+    batches that fit one CTA per sequence the small-batch kernel."""
+    import types
+    # cluster sizes at the bench's vocabularies and at the limits
+    assert bench.ee_cluster_size(32000 * 2 // 16) == 1
+    assert bench.ee_cluster_size(20000 * 4 // 16) == 1
+    assert bench.ee_cluster_size(65536 * 2 // 16) == 2
+    assert bench.ee_cluster_size(128256 * 2 // 16) == 4
+    assert bench.ee_cluster_size(152064 * 4 // 16) == 8
+    assert bench.ee_cluster_size(400000 * 2 // 16) == 0
+    nv = 6144  # a slice of 6144 vectors: 192 KiB of rows + 6 checkpoint groups > 200 KiB
+    assert bench.ee_cluster_size(8 * nv) == 0 and bench.ee_cluster_size(8 * 6000) == 8
+    want = {"tiny_sample_f32_B4_K4_V1000": "small_batch"}
+    for name, spec in W.WORKLOADS.items():
+        if spec["mode"] != W.MODE_SAMPLE or spec["K"] == 0:
+            continue
+        inp = types.SimpleNamespace(B=spec["B"], K=spec["K"], V=spec["V"],
+                                    target=torch.empty(0, dtype=spec["dtype"]))
+        assert bench.early_exit_schedule(inp) == want.get(name, "cluster"), name
+    inp = types.SimpleNamespace(B=4, K=2, V=400000, target=torch.empty(0, dtype=torch.bfloat16))
+    assert bench.early_exit_schedule(inp) == "two_phase"
