@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-workload table and the CPU baseline")
     ap.add_argument("--line", default=None,
-                    help="time one contrastive-verify, rejection-cut or <workload>+draft_sample line alone "
+                    help="time one contrastive-verify, rejection-cut, <workload>+draft_sample or "
+                         "<workload>+early_exit line alone "
                          "(--steps launches) and print its line")
     return ap.parse_args()
 
@@ -180,6 +181,8 @@ KERNEL_SOURCES = {
     "scd_row_kernel": ["verify_scd.cu", "sample_common.cuh", "device_common.cuh", "launch.h"],
     "row_sample_kernel": ["verify_draft_sample.cu", "sample_common.cuh", "device_common.cuh",
                           "launch.h"],
+    "ee_cluster_kernel": ["verify_sample_ee.cu", "sample_common.cuh", "device_common.cuh",
+                          "launch.h", "launch_ee.h"],
 }
 
 
@@ -750,9 +753,15 @@ def early_exit_line(binding, inp, steps, dev, l2, peak, parallel_sec):
         read = 2 * inp.B * inp.V * s + small + (inp.algorithmic_bytes() if full_ran else 0)
     del launch
     torch.cuda.empty_cache()
+    kernel = "ee_cluster_kernel" if schedule == "cluster" else None
     return {"us_per_step": sec * 1e6, "positions_per_s": inp.B * inp.K / sec, "schedule": schedule,
             "bytes_read": read, "GB_per_s": read / sec / 1e9, "frac_hbm": read / sec / 1e9 / peak,
-            "full_verify_ran": full_ran, "speedup_vs_sampling_mode": parallel_sec / sec}
+            "full_verify_ran": full_ran, "speedup_vs_sampling_mode": parallel_sec / sec,
+            "roofline": {"bound": "hbm", "achieved": read / sec / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": read / sec / 1e9 / peak, "algorithmic_bytes_per_launch": read,
+                         "kernel": kernel,
+                         "traffic": committed_traffic(inp.name + "+early_exit", kernel)
+                         if kernel else None}}
 
 
 def cpu_baseline(inp, budget_s=10.0):
@@ -859,6 +868,12 @@ def run_line(args):
     elif args.line.endswith("+draft_sample") and args.line[:-len("+draft_sample")] in W.WORKLOADS:
         inp = W.workload(args.line[:-len("+draft_sample")])
         res = draft_sample_line(binding, inp, args.steps, dev, l2, peak)
+    elif args.line.endswith("+early_exit") and args.line[:-len("+early_exit")] in W.WORKLOADS:
+        inp = W.workload(args.line[:-len("+early_exit")])
+        R, stream, launch, _ = device_setup(binding, inp, dev, l2)
+        sec = GraphTimer(launch, args.steps, 5, stream, dev).per_launch()
+        del launch
+        res = early_exit_line(binding, inp, args.steps, dev, l2, peak, sec)
     else:
         raise SystemExit(f"unknown line {args.line!r}")
     print(json.dumps({"line": args.line, **res}))
