@@ -143,7 +143,7 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
     const bool pair = i < K;
     const uint32_t par = static_cast<uint32_t>(i & 1);  // every barrier completes once per position
     // ---- stage position i's slices (thread 0) -----------------------------
-    if (tid == 0) {
+    if (tid == 0 && !s_fail) {
       // the CTA's reads of the previous position are done (barrier below):
       // order them before the async proxy writes the same shared memory
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -172,8 +172,10 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
 
     // ---- (1) online normalisers as the copies land, one exchange ----------
     RowAcc At{-INFINITY, 0.f}, Ad{-INFINITY, 0.f};
-    bool ok = true;
-    for (int c = 0; c < nch; ++c) {
+    // after a copy that never landed the barriers' phases are lost: every
+    // later wait is skipped (the outputs are unspecified, the status says so)
+    bool ok = s_fail == 0;
+    for (int c = 0; ok && c < nch; ++c) {
       if (!mbar_wait_sleep(&bar_t[c], par) || (pair && !mbar_wait_sleep(&bar_d[c], par))) {
         ok = false;
         break;
