@@ -11,7 +11,7 @@
 //     all K accepted the target supplies token K+1, drawn from p_K.
 //
 // Design: each CTA stages its slice of the position's target row and draft
-// row in shared memory (TMA bulk copies of 16 KiB, one mbarrier each), so a
+// row in shared memory (TMA bulk copies of 32 KiB, one mbarrier each), so a
 // row crosses HBM once and the draw at the rejected position reads nothing
 // again.  Per position: (1) both rows' online normalisers as the copies land
 // (max and sum of 2^(x*s - offset)), exchanged over the cluster through DSMEM
@@ -42,7 +42,7 @@ namespace {
 constexpr int kThreadsE = 512;
 constexpr int kWarpsE = kThreadsE / 32;
 constexpr int kMaxCE = 8;
-constexpr int kChunkE = 1024;                  // vectors per bulk copy (16 KiB)
+constexpr int kChunkE = 2048;                  // vectors per bulk copy (32 KiB)
 constexpr long long kBudgetE = 200 * 1024;     // slices and checkpoints of one CTA
 constexpr int kMaxChunksE = static_cast<int>(kBudgetE / 2 / 16 / kChunkE) + 1;
 constexpr int kGroupE = 4;                     // 32-vector steps between a lane's checkpoints
@@ -181,28 +181,29 @@ ee_cluster_kernel(VerifyArgs a, long long nvec) {
         break;
       }
       const int c0 = c * kChunkE, cend = min(c0 + kChunkE, nv);
-      if (cend - c0 == kChunkE) {  // a full chunk: two vectors of each row a thread
-        static_assert(kChunkE == 2 * kThreadsE, "two vectors of each row a thread");
-        const uint4 wt[2] = {st[c0 + tid], st[c0 + kThreadsE + tid]};
-        acc_vectors_full<E>(At, wt, s);
-        if (pair) {
-          const uint4 wd[2] = {sd[c0 + tid], sd[c0 + kThreadsE + tid]};
-          acc_vectors_full<E>(Ad, wd, s);
+      if (cend - c0 == kChunkE) {  // a full chunk: pairs of vectors of each row a thread
+#pragma unroll
+        for (int k = 0; k < kChunkE / kThreadsE; k += 2) {
+          const uint4 wt[2] = {st[c0 + k * kThreadsE + tid], st[c0 + (k + 1) * kThreadsE + tid]};
+          acc_vectors_full<E>(At, wt, s);
+          if (pair) {
+            const uint4 wd[2] = {sd[c0 + k * kThreadsE + tid], sd[c0 + (k + 1) * kThreadsE + tid]};
+            acc_vectors_full<E>(Ad, wd, s);
+          }
         }
       } else {
-        const int v = c0 + tid;
-        const int n2 = (v < cend ? 1 : 0) + (v + kThreadsE < cend ? 1 : 0);
-        uint4 wt[2], wd[2];
-        if (n2 > 0) {
+        for (int v = c0 + tid; v < cend; v += 2 * kThreadsE) {
+          const int n2 = 1 + (v + kThreadsE < cend ? 1 : 0);
+          uint4 wt[2], wd[2];
           wt[0] = st[v];
           if (pair) wd[0] = sd[v];
+          if (n2 > 1) {
+            wt[1] = st[v + kThreadsE];
+            if (pair) wd[1] = sd[v + kThreadsE];
+          }
+          acc_vectors<E>(At, wt, n2, s);
+          if (pair) acc_vectors<E>(Ad, wd, n2, s);
         }
-        if (n2 > 1) {
-          wt[1] = st[v + kThreadsE];
-          if (pair) wd[1] = sd[v + kThreadsE];
-        }
-        acc_vectors<E>(At, wt, n2, s);
-        if (pair) acc_vectors<E>(Ad, wd, n2, s);
       }
     }
     warp_merge_scaled(At.ms, At.z);
